@@ -1,0 +1,372 @@
+// Grouped block-scaled GEMMs of the experts forward on tcgen05 tensor cores.
+//
+// The deepgemm excerpt (deepgemm.py lines 678-714) runs the experts as two
+// grouped matmuls with FP8 activations and FP8 or FP4 expert weights
+// (grouped_fp8_fp4_matmul_nt: both operands K-major). This kernel computes,
+// for every expert e and every 128-row tile of its group in the padded
+// grouped layout, one 128 x 256 output tile:
+//
+//   D[r, n] = sum_k deq(A)[r, k] * deq(W_e)[n, k]
+//
+// GEMM1 (A = quantized hidden rows, W = interleaved gate_up) ends with the
+// SwiGLU epilogue: optional clamp (swiglu_limit, "absent -> unclamped" in the
+// Mega MoE docstring), act = silu(gate) * up in fp32, requantization of act
+// in 1x128 blocks with the same power-of-two e4m3 rule as the input.
+// GEMM2 (A = act, W = down_proj) multiplies each row by the routing weight of
+// its slot and stores fp32 rows for the deterministic combine.
+//
+// Pipeline (one persistent CTA per SM, 10 warps):
+//   warp 0      TMA producer: A tile 128x128 B, W tile 256x128 B (+ FP4 scale
+//               blocks) per 128-K stage into a 4-deep shared-memory ring;
+//   warp 1      allocates tensor memory and issues tcgen05.mma (one thread);
+//   warps 2..9  two epilogue warpgroups, each owning 128 of the 256 columns.
+// FP8 weights carry an fp32 scale per 128x128 block, which the block-scaled
+// MMA cannot apply (it takes power-of-two scale bytes), so each 128-K block
+// is multiplied without scaling into one of two TMEM partial buffers and the
+// epilogue warps promote it into fp32 registers with 2^e_act * s_w.
+// FP4 weights use the hardware block-scaled MMA (kind::mxf8f6f4, one UE8M0
+// byte per 32 K for both operands); the activation's 1x128 exponent is
+// replicated into four bytes, and the scale blocks are copied shared ->
+// tensor memory with tcgen05.cp before the stage's MMAs.
+#include <cuda_bf16.h>
+
+#include "act_quant.cuh"
+#include "moe_internal.cuh"
+#include "ptx.cuh"
+
+namespace bsmoe {
+
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kThreads = 320;
+constexpr int kEpiThreads = 256;
+constexpr uint32_t kTileABytes = kBlockM * kBlockK;  // 16 KB
+constexpr uint32_t kTileBBytes = kBlockN * kBlockK;  // 32 KB (FP4 is unpacked to 1 B/elem in smem)
+constexpr uint32_t kSfaBytes = 512;
+constexpr uint32_t kSfbBytes = 1024;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfTmemCol = 256;  // FP4: per stage 4 SFA + 8 SFB columns from here
+
+struct __align__(1024) Smem {
+  uint8_t a[kStages][kTileABytes];
+  uint8_t b[kStages][kTileBBytes];
+  uint8_t sfa[kStages][kSfaBytes];
+  uint8_t sfb[kStages][kSfbBytes];
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  float amax_x[2][2][kBlockM];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct TileCoord {
+  int e, mt, nt, row0, valid;
+};
+
+// idx -> (expert, m tile, n tile). Tiles are ordered expert-major, then by n
+// tile, with the expert's m tiles fastest, so CTAs running at the same time
+// share weight tiles through L2.
+__device__ __forceinline__ TileCoord decode_tile(int idx, int E, int NT, const int32_t* __restrict__ mt_off,
+                                                 const int32_t* __restrict__ counts,
+                                                 const int32_t* __restrict__ padded_offsets) {
+  int lo = 0, hi = E;  // find e with NT*mt_off[e] <= idx < NT*mt_off[e+1]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (NT * __ldg(mt_off + mid) <= idx) lo = mid; else hi = mid;
+  }
+  TileCoord c;
+  c.e = lo;
+  const int m_e = __ldg(mt_off + lo + 1) - __ldg(mt_off + lo);
+  const int local = idx - NT * __ldg(mt_off + lo);
+  c.nt = local / m_e;
+  c.mt = local % m_e;
+  c.row0 = __ldg(padded_offsets + lo) + kBlockM * c.mt;
+  c.valid = min(kBlockM, __ldg(counts + lo) - kBlockM * c.mt);
+  return c;
+}
+
+// Barrier over the two epilogue warpgroups that also ORs a flag across them,
+// so that both take the same decision to stop after a failed wait.
+__device__ __forceinline__ bool epi_barrier_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 1, %2, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "n"(kEpiThreads)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+template <int FMT, bool GEMM1>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                    const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const GemmGeom g = args.g;
+  const int KB = g.KB, NT = g.NT;
+  const int32_t* mt_off = args.tiles + kTilesHdr;
+  const int total_tiles = __ldg(args.tiles) * NT;
+  volatile int* abort_flag = &sm.abort_flag;
+
+  if (tid == 0) {
+    sm.abort_flag = 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.tfull[b], 1);
+      mbar_init(&sm.tempty[b], kEpiThreads / 32);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = sm.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmap_a);
+      tma_prefetch_desc(&tmap_b);
+      // The FP4 tile lands unpacked (16 codes per 16 bytes) but the copy's
+      // transaction count is the packed global size.
+      const uint32_t bytes = (FMT == MOE_W_FP4) ? kTileABytes + kTileBBytes / 2 + kSfaBytes + kSfbBytes
+                                                : kTileABytes + kTileBBytes;
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int idx = blockIdx.x; idx < total_tiles && !*abort_flag; idx += gridDim.x) {
+        const TileCoord c = decode_tile(idx, args.E, NT, mt_off, args.counts, args.padded_offsets);
+        const int wrow = c.e * g.Np + c.nt * kBlockN;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&sm.empty[stage], phase ^ 1, abort_flag)) break;
+          mbar_arrive_expect_tx(&sm.full[stage], bytes);
+          tma_load_2d(sm.a[stage], &tmap_a, &sm.full[stage], kb * kBlockK, c.row0);
+          tma_load_2d(sm.b[stage], &tmap_b, &sm.full[stage], kb * kBlockK, wrow);
+          if constexpr (FMT == MOE_W_FP4) {
+            bulk_load(sm.sfa[stage], args.a_sf + (static_cast<size_t>(c.row0 / kBlockM) * KB + kb) * kSfaBytes,
+                      kSfaBytes, &sm.full[stage]);
+            bulk_load(sm.sfb[stage],
+                      args.w_scale + ((static_cast<size_t>(c.e) * NT + c.nt) * KB + kb) * kSfbBytes, kSfbBytes,
+                      &sm.full[stage]);
+          }
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int buf = 0;
+      uint32_t bphase = 0;
+      for (int idx = blockIdx.x; idx < total_tiles && !*abort_flag; idx += gridDim.x) {
+        if constexpr (FMT == MOE_W_FP8) {
+          constexpr uint32_t idesc = idesc_f8f6f4(0, 0, kBlockM, kBlockN);
+          for (int kb = 0; kb < KB; ++kb) {
+            if (!mbar_wait(&sm.full[stage], phase, abort_flag)) break;
+            if (!mbar_wait(&sm.tempty[buf], bphase ^ 1, abort_flag)) break;
+            tc_fence_after();
+            const uint64_t ad = smem_desc(smem_u32(sm.a[stage]), 16, 1024, kSwizzle128B);
+            const uint64_t bd = smem_desc(smem_u32(sm.b[stage]), 16, 1024, kSwizzle128B);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              mma_f8f6f4(tbase + buf * kBlockN, ad + 2 * j, bd + 2 * j, idesc, j > 0 ? 1u : 0u);
+            mma_commit(&sm.empty[stage]);
+            mma_commit(&sm.tfull[buf]);
+            if (++stage == kStages) { stage = 0; phase ^= 1; }
+            buf ^= 1;
+            if (buf == 0) bphase ^= 1;
+          }
+        } else {
+          if (!mbar_wait(&sm.tempty[0], bphase ^ 1, abort_flag)) break;
+          tc_fence_after();
+          for (int kb = 0; kb < KB; ++kb) {
+            if (!mbar_wait(&sm.full[stage], phase, abort_flag)) break;
+            tc_fence_after();
+            const uint32_t sfa_col = kSfTmemCol + stage * 12;
+            const uint32_t sfb_col = sfa_col + 4;
+            tmem_cp_32x128b_warpx4(tbase + sfa_col, smem_desc(smem_u32(sm.sfa[stage]), 0, 128, kSwizzleNone));
+            tmem_cp_32x128b_warpx4(tbase + sfb_col, smem_desc(smem_u32(sm.sfb[stage]), 0, 128, kSwizzleNone));
+            tmem_cp_32x128b_warpx4(tbase + sfb_col + 4,
+                                   smem_desc(smem_u32(sm.sfb[stage] + 512), 0, 128, kSwizzleNone));
+            const uint64_t ad = smem_desc(smem_u32(sm.a[stage]), 16, 1024, kSwizzle128B);
+            const uint64_t bd = smem_desc(smem_u32(sm.b[stage]), 16, 1024, kSwizzle128B);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              mma_mxf8f6f4(tbase, ad + 2 * j, bd + 2 * j, idesc_mxf8f6f4(0, 5, kBlockM, kBlockN, j, j),
+                           tbase + sfa_col, tbase + sfb_col, (kb > 0 || j > 0) ? 1u : 0u);
+            mma_commit(&sm.empty[stage]);
+            if (++stage == kStages) { stage = 0; phase ^= 1; }
+          }
+          mma_commit(&sm.tfull[0]);
+          bphase ^= 1;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int wg = (warp - 2) / 4;          // column half of the tile
+    const int quarter = warp & 3;           // TMEM lane quarter this warp may access
+    const int m = quarter * 32 + lane;      // tile row owned by this thread
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    int buf = 0;
+    uint32_t bphase = 0;
+    int tile_parity = 0;
+    const float limit = args.swiglu_limit;
+    const bool clamp = limit > 0.f && limit < INFINITY;
+    for (int idx = blockIdx.x; idx < total_tiles && !*abort_flag; idx += gridDim.x) {
+      const TileCoord c = decode_tile(idx, args.E, NT, mt_off, args.counts, args.padded_offsets);
+      float acc[128];
+      bool ok = true;
+      if constexpr (FMT == MOE_W_FP8) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) acc[i] = 0.f;
+        const uint32_t* sfw = reinterpret_cast<const uint32_t*>(args.a_sf);
+        const float* wsc = reinterpret_cast<const float*>(args.w_scale) +
+                           (static_cast<size_t>(c.e) * (g.Np / 32) + (c.nt * kBlockN + wg * 128) / 32) * KB;
+        for (int kb = 0; kb < KB; ++kb) {
+          const uint32_t word = __ldg(sfw + sf_word_index(c.row0 + m, kb, KB));
+          float sw[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) sw[q] = __ldg(wsc + q * KB + kb);
+          const float sa = exp2f(static_cast<float>(static_cast<int>(word & 0xFF) - 127));
+          if (!mbar_wait(&sm.tfull[buf], bphase, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tbase + lane_base + buf * kBlockN + wg * 128 + q * 32, r);
+            tmem_wait_ld();
+            const float sc = sa * sw[q];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[q * 32 + j] = fmaf(__uint_as_float(r[j]), sc, acc[q * 32 + j]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.tempty[buf]);
+          buf ^= 1;
+          if (buf == 0) bphase ^= 1;
+        }
+      } else {
+        if (!mbar_wait(&sm.tfull[0], bphase, abort_flag)) ok = false;
+        if (ok) {
+          tc_fence_after();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tbase + lane_base + wg * 128 + q * 32, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[q * 32 + j] = __uint_as_float(r[j]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.tempty[0]);
+          bphase ^= 1;
+        }
+      }
+      const int row = c.row0 + m;
+      if constexpr (GEMM1) {
+        // acc[0..63] = gate, acc[64..127] = up of intermediate columns
+        // j = 128 nt + 64 wg + i.
+        float amax = 0.f;
+        if (ok) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            float gt = acc[i], up = acc[64 + i];
+            if (clamp) {
+              gt = fminf(gt, limit);
+              up = fminf(fmaxf(up, -limit), limit);
+            }
+            const float a = silu_mul(gt, up);
+            acc[i] = a;
+            amax = fmaxf(amax, fabsf(a));
+          }
+        }
+        sm.amax_x[tile_parity][wg][m] = amax;
+        // Every epilogue thread reaches this barrier once per tile, failed
+        // wait or not; all of them stop together if any wait failed.
+        if (epi_barrier_any(!ok)) break;
+        amax = fmaxf(sm.amax_x[tile_parity][0][m], sm.amax_x[tile_parity][1][m]);
+        tile_parity ^= 1;
+        const int e = act_exponent(amax);
+        const float s = exp2_neg(e);
+        if (m < c.valid) {
+          uint8_t* dst = args.out_q + static_cast<size_t>(row) * args.out_cols + c.nt * 128 + wg * 64;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 pk;
+            pk.x = pack4_e4m3(acc[16 * v + 0] * s, acc[16 * v + 1] * s, acc[16 * v + 2] * s, acc[16 * v + 3] * s);
+            pk.y = pack4_e4m3(acc[16 * v + 4] * s, acc[16 * v + 5] * s, acc[16 * v + 6] * s, acc[16 * v + 7] * s);
+            pk.z = pack4_e4m3(acc[16 * v + 8] * s, acc[16 * v + 9] * s, acc[16 * v + 10] * s, acc[16 * v + 11] * s);
+            pk.w = pack4_e4m3(acc[16 * v + 12] * s, acc[16 * v + 13] * s, acc[16 * v + 14] * s, acc[16 * v + 15] * s);
+            *reinterpret_cast<uint4*>(dst + 16 * v) = pk;
+          }
+          if (wg == 0)
+            reinterpret_cast<uint32_t*>(args.out_sf)[sf_word_index(row, c.nt, args.out_blocks)] =
+                static_cast<uint32_t>(e + 127) * 0x01010101u;
+        }
+      } else {
+        if (!ok) break;
+        if (m < c.valid) {
+          const int slot = __ldg(args.row_slot + row);
+          const float wgt = __ldg(args.topk_w + slot);
+          const int col0 = c.nt * kBlockN + wg * 128;
+          float* dst = args.out_y + static_cast<size_t>(row) * args.H + col0;
+#pragma unroll
+          for (int v = 0; v < 32; ++v) {
+            if (col0 + 4 * v < args.H) {
+              float4 o = make_float4(acc[4 * v] * wgt, acc[4 * v + 1] * wgt, acc[4 * v + 2] * wgt,
+                                     acc[4 * v + 3] * wgt);
+              *reinterpret_cast<float4*>(dst + 4 * v) = o;
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tbase, kTmemCols);
+  if (tid == 0 && sm.abort_flag) atomicOr(args.status, MOE_DEV_TIMEOUT);
+}
+
+template <int FMT, bool GEMM1>
+cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args, int num_sms,
+                       cudaStream_t st) {
+  auto kern = grouped_gemm_kernel<FMT, GEMM1>;
+  const int smem = static_cast<int>(sizeof(Smem)) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<num_sms, kThreads, smem, st>>>(ta, tb, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(int fmt, bool is_gemm1, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args,
+                        int num_sms, cudaStream_t st) {
+  if (fmt == MOE_W_FP8)
+    return is_gemm1 ? launch_one<MOE_W_FP8, true>(ta, tb, args, num_sms, st)
+                    : launch_one<MOE_W_FP8, false>(ta, tb, args, num_sms, st);
+  return is_gemm1 ? launch_one<MOE_W_FP4, true>(ta, tb, args, num_sms, st)
+                  : launch_one<MOE_W_FP4, false>(ta, tb, args, num_sms, st);
+}
+
+}  // namespace bsmoe

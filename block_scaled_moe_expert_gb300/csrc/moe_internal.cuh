@@ -1,0 +1,84 @@
+// Internal declarations shared by the kernels and the C-ABI host layer.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/moe_experts.h"
+
+namespace bsmoe {
+
+constexpr int kBlockM = 128;     // token rows per tile (tcgen05 M)
+constexpr int kBlockN = 256;     // weight rows per tile (tcgen05 N)
+constexpr int kBlockK = 128;     // K per pipeline stage (= activation block)
+constexpr int kRowAlign = 128;   // group alignment of the padded layout
+constexpr int kMaxExperts = 512;
+constexpr int kMaxTopK = 32;
+constexpr int kGroup = 64;       // gate/up interleave granularity
+constexpr int kSfChunkBytes = 512;  // scale words of 128 rows x one K block
+
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Geometry of one GEMM operand set, shared by host and device.
+struct GemmGeom {
+  int Kp;      // padded K (multiple of 128)
+  int KB;      // Kp / 128
+  int Np;      // padded N of the prepared weights per expert (multiple of 256)
+  int NT;      // Np / 256
+  int N;       // logical N (2I for GEMM1, H for GEMM2)
+};
+
+// Prepared weight layout (one of w13 / w2).
+struct PrepLayout {
+  size_t codes_off, codes_bytes;  // u8 [E][Np][Kp] (FP8) or [E][Np][Kp/2] (FP4)
+  size_t scale_off, scale_bytes;  // FP8: f32 [E][Np/32][KB]; FP4: u32 chunks [E][NT][KB][256]
+  size_t total;
+};
+
+PrepLayout prep_layout(int fmt, int E, const GemmGeom& g);
+GemmGeom geom_w13(int H, int I);
+GemmGeom geom_w2(int H, int I);
+
+struct WsLayout {
+  moe_workspace_layout pub;
+  int S, M, max_m_tiles;
+};
+bool ws_layout(int fmt, int T, int H, int I, int E, int K, WsLayout* out);
+
+// Offsets inside the int32 "tiles" region.
+constexpr int kTilesHdr = 16;  // [0] = number of m-tiles; [16 + e] = m-tile offset of expert e (E+1)
+
+// ---------------------------------------------------------------- launches
+cudaError_t launch_route(const int32_t* topk_idx, int S, int E, const WsLayout& L, uint8_t* ws, cudaStream_t st);
+cudaError_t launch_quant(const void* hidden, int T, int H, int K, const WsLayout& L, uint8_t* ws, cudaStream_t st);
+cudaError_t launch_combine(const float* y, const int32_t* inv, int T, int H, int K, void* out, cudaStream_t st);
+cudaError_t launch_prepare(int fmt, int E, int H, int I, const void* w13, const void* w13s, const void* w2,
+                           const void* w2s, uint8_t* p13, uint8_t* p2, cudaStream_t st);
+
+struct GemmArgs {
+  // operands
+  const uint8_t* a_sf;        // activation scale words (chunk layout)
+  const uint8_t* w_scale;     // prepared weight scales
+  const int32_t* counts;
+  const int32_t* padded_offsets;
+  const int32_t* tiles;
+  const int32_t* row_slot;
+  const float* topk_w;
+  uint32_t* status;
+  // outputs
+  uint8_t* out_q;             // GEMM1: e4m3 act [M][act_cols]
+  uint8_t* out_sf;            // GEMM1: act scale words
+  float* out_y;               // GEMM2: f32 [M][H]
+  int out_cols;               // GEMM1: act_cols (= Kp of GEMM2); GEMM2: H
+  int out_blocks;             // GEMM1: act_blocks
+  int E, I, H;
+  float swiglu_limit;         // > 0 and finite: clamp
+  GemmGeom g;
+};
+
+cudaError_t launch_gemm(int fmt, bool is_gemm1, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                        const GemmArgs& args, int num_sms, cudaStream_t st);
+
+}  // namespace bsmoe

@@ -1,0 +1,164 @@
+// One-shot weight transform into the kernel layout.
+//
+// The Mega MoE forward (deepgemm.py error page, lines 857-893) packs the
+// UE8M0 scale factors and interleaves the L1/L2 weights once, before the
+// first forward. This is the same idea made explicit:
+//   * gate_up rows are interleaved in 64-row groups so that one 256-row
+//     N tile t holds gate and up rows of the same 128 intermediate columns:
+//       tile rows [  0, 64) gate j = 128t + r      [ 64,128) up j = 128t + r - 64
+//       tile rows [128,192) gate j = 128t + r - 64 [192,256) up j = 128t + r - 128
+//     (up j is original row I + j); rows with j >= I are zero;
+//   * K is padded to a multiple of 128 and N to a multiple of 256 with zeros;
+//   * FP8 block scales become one fp32 per (32 prepared rows, 128-K block);
+//   * FP4 UE8M0 scales become, per (expert, N tile, K block), the 1 KB image
+//     of the two 128-row scale blocks that tcgen05.cp copies into tensor
+//     memory: word(row r) at 4 * (r % 32) + r / 32, byte j = scale of the
+//     j-th 32-wide K chunk.
+#include "moe_internal.cuh"
+
+namespace bsmoe {
+
+GemmGeom geom_w13(int H, int I) {
+  GemmGeom g;
+  g.Kp = ceil_div(H, 128) * 128;
+  g.KB = g.Kp / 128;
+  g.Np = 2 * ceil_div(I, 128) * 128;
+  g.NT = g.Np / 256;
+  g.N = 2 * I;
+  return g;
+}
+
+GemmGeom geom_w2(int H, int I) {
+  GemmGeom g;
+  g.Kp = ceil_div(I, 128) * 128;
+  g.KB = g.Kp / 128;
+  g.Np = ceil_div(H, 256) * 256;
+  g.NT = g.Np / 256;
+  g.N = H;
+  return g;
+}
+
+PrepLayout prep_layout(int fmt, int E, const GemmGeom& g) {
+  PrepLayout p;
+  const size_t row_bytes = (fmt == MOE_W_FP8) ? g.Kp : g.Kp / 2;
+  p.codes_off = 0;
+  p.codes_bytes = static_cast<size_t>(E) * g.Np * row_bytes;
+  p.scale_off = align_up(p.codes_bytes, 1024);
+  if (fmt == MOE_W_FP8)
+    p.scale_bytes = static_cast<size_t>(E) * (g.Np / 32) * g.KB * sizeof(float);
+  else
+    p.scale_bytes = static_cast<size_t>(E) * g.NT * g.KB * 256 * sizeof(uint32_t);
+  p.total = align_up(p.scale_off + p.scale_bytes, 1024);
+  return p;
+}
+
+namespace {
+
+// Prepared row -> original row, or -1 for a zero row.
+__device__ __forceinline__ int orig_row(bool is_w13, int p, int I, int H) {
+  if (!is_w13) return p < H ? p : -1;
+  const int t = p / 256, r = p % 256;
+  const int q = r / 64;
+  const int j = 128 * t + 64 * (q / 2) + (r % 64);
+  if (j >= I) return -1;
+  return (q & 1) ? I + j : j;
+}
+
+// Copy one prepared row of codes (row_bytes = Kp or Kp/2), zero padded.
+__global__ void prep_codes_kernel(bool is_w13, const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int Np,
+                                  int src_row_bytes, int dst_row_bytes, int src_rows, int I, int H) {
+  const int p = blockIdx.x, e = blockIdx.y;
+  const int o = orig_row(is_w13, p, I, H);
+  uint8_t* d = dst + (static_cast<size_t>(e) * Np + p) * dst_row_bytes;
+  const uint8_t* s = (o >= 0) ? src + (static_cast<size_t>(e) * src_rows + o) * src_row_bytes : nullptr;
+  for (int c = threadIdx.x * 16; c < dst_row_bytes; c += blockDim.x * 16) {
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (s != nullptr && c < src_row_bytes) {
+      if (c + 16 <= src_row_bytes && (src_row_bytes % 16) == 0) {
+        v = *reinterpret_cast<const uint4*>(s + c);
+      } else {
+        uint8_t tmp[16];
+        for (int i = 0; i < 16; ++i) tmp[i] = (c + i < src_row_bytes) ? s[c + i] : 0;
+        v = *reinterpret_cast<uint4*>(tmp);
+      }
+    }
+    *reinterpret_cast<uint4*>(d + c) = v;
+  }
+}
+
+// FP8 scales: out[e][g][kb] = scale[e][orig(32 g) / 128][kb] (0 for zero rows).
+__global__ void prep_scale_fp8_kernel(bool is_w13, const float* __restrict__ src, float* __restrict__ dst, int Np,
+                                      int KB, int src_rb, int src_kb, int I, int H) {
+  const int e = blockIdx.y;
+  const int n_groups = Np / 32;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_groups * KB; i += gridDim.x * blockDim.x) {
+    const int g = i / KB, kb = i % KB;
+    const int o = orig_row(is_w13, g * 32, I, H);
+    float v = 0.f;
+    if (o >= 0 && kb < src_kb) v = src[(static_cast<size_t>(e) * src_rb + o / 128) * src_kb + kb];
+    dst[(static_cast<size_t>(e) * n_groups + g) * KB + kb] = v;
+  }
+}
+
+// FP4 scales into the tensor-memory staging image (see the file comment).
+__global__ void prep_scale_fp4_kernel(bool is_w13, const uint8_t* __restrict__ src, uint32_t* __restrict__ dst,
+                                      int NT, int KB, int src_cols, int I, int H) {
+  const int e = blockIdx.y;
+  const int total = NT * KB * 256;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    const int w = i % 256;
+    const int kb = (i / 256) % KB;
+    const int nt = i / (256 * KB);
+    const int half = w / 128, wi = w % 128;
+    const int rr = 32 * (wi % 4) + wi / 4;  // inverse of word(r) = 4 (r % 32) + r / 32
+    const int p = nt * 256 + half * 128 + rr;
+    const int o = orig_row(is_w13, p, I, H);
+    uint32_t word = 0;
+    for (int j = 0; j < 4; ++j) {
+      const int c = kb * 4 + j;
+      uint32_t b = 127;
+      if (o >= 0 && c < src_cols) {
+        const int src_rows = is_w13 ? 2 * I : H;
+        b = src[(static_cast<size_t>(e) * src_rows + o) * src_cols + c];
+      }
+      word |= b << (8 * j);
+    }
+    dst[static_cast<size_t>(e) * total + i] = word;
+  }
+}
+
+cudaError_t prep_one(int fmt, bool is_w13, int E, int H, int I, const void* w, const void* ws, uint8_t* out,
+                     cudaStream_t st) {
+  const GemmGeom g = is_w13 ? geom_w13(H, I) : geom_w2(H, I);
+  const PrepLayout L = prep_layout(fmt, E, g);
+  const int src_rows = is_w13 ? 2 * I : H;
+  const int src_k = is_w13 ? H : I;
+  const int src_row_bytes = (fmt == MOE_W_FP8) ? src_k : src_k / 2;
+  const int dst_row_bytes = (fmt == MOE_W_FP8) ? g.Kp : g.Kp / 2;
+  (void)src_rows;
+  prep_codes_kernel<<<dim3(g.Np, E), 128, 0, st>>>(is_w13, static_cast<const uint8_t*>(w), out + L.codes_off, g.Np,
+                                            src_row_bytes, dst_row_bytes, is_w13 ? 2 * I : H, I, H);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  if (fmt == MOE_W_FP8) {
+    prep_scale_fp8_kernel<<<dim3(64, E), 256, 0, st>>>(is_w13, static_cast<const float*>(ws),
+                                                reinterpret_cast<float*>(out + L.scale_off), g.Np, g.KB,
+                                                ceil_div(src_rows, 128), ceil_div(src_k, 128), I, H);
+  } else {
+    prep_scale_fp4_kernel<<<dim3(64, E), 256, 0, st>>>(is_w13, static_cast<const uint8_t*>(ws),
+                                                reinterpret_cast<uint32_t*>(out + L.scale_off), g.NT, g.KB,
+                                                src_k / 32, I, H);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prepare(int fmt, int E, int H, int I, const void* w13, const void* w13s, const void* w2,
+                           const void* w2s, uint8_t* p13, uint8_t* p2, cudaStream_t st) {
+  cudaError_t e = prep_one(fmt, true, E, H, I, w13, w13s, p13, st);
+  if (e != cudaSuccess) return e;
+  return prep_one(fmt, false, E, H, I, w2, w2s, p2, st);
+}
+
+}  // namespace bsmoe

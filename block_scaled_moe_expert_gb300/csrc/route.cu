@@ -1,0 +1,178 @@
+// Routing: flatten the top-k pairs, count them per expert and place them in a
+// padded grouped layout with a stable counting sort.
+//
+// Follows "fp8_grouped_mm_experts_forward" (finegrained_fp8.py excerpt):
+// flatten (slot s = t*K + k), sort by expert id, gather rows by s // K; and
+// the sorted_to_padded map of the deepgemm excerpt (lines 678-684). The sort
+// is stable (equal ids keep ascending slot order) and a skipped slot (-1, or
+// an id outside [-1, E), which also raises MOE_DEV_BAD_EXPERT_ID) takes key E
+// so it sorts after every group.
+//
+// One CTA of 32 warps. Warp w owns a contiguous range of slots and walks it
+// 32 slots at a time; __match_any_sync groups equal keys inside a step, so a
+// slot's rank is (#equal keys in earlier warps) + (#equal keys earlier in its
+// own warp), which is exactly the stable order. No data atomics are used:
+// the result is deterministic.
+#include "moe_internal.cuh"
+
+namespace bsmoe {
+
+namespace {
+
+constexpr int kWarps = 32;
+constexpr int kThreads = kWarps * 32;
+
+__device__ __forceinline__ int slot_key(const int32_t* idx, int s, int E, uint32_t* status) {
+  int v = __ldg(idx + s);
+  if (v >= 0 && v < E) return v;
+  if (v != -1) atomicOr(status, MOE_DEV_BAD_EXPERT_ID);
+  return E;
+}
+
+// Block-wide exclusive scan of one int per thread (1024 threads).
+__device__ __forceinline__ int block_excl_scan(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_sums[lane];
+    int ws = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, ws, o);
+      if (lane >= o) ws += y;
+    }
+    warp_sums[lane] = ws - w;  // exclusive
+    if (lane == 31) *total = ws;
+  }
+  __syncthreads();
+  int r = warp_sums[warp] + x - v;
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+route_kernel(const int32_t* __restrict__ idx, int S, int E, int M, int32_t* __restrict__ counts,
+             int32_t* __restrict__ offsets, int32_t* __restrict__ padded_offsets, int32_t* __restrict__ perm,
+             int32_t* __restrict__ inv, int32_t* __restrict__ row_slot, int32_t* __restrict__ tiles,
+             uint32_t* __restrict__ status) {
+  extern __shared__ int hist[];  // [kWarps][E + 1]
+  __shared__ int warp_sums[32];
+  __shared__ int tot[3];
+  __shared__ int s_off[kMaxExperts + 1];
+  __shared__ int s_pad[kMaxExperts + 1];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int stride = E + 1;
+  // The status word reflects the most recent forward on this workspace.
+  if (tid == 0) *status = 0u;
+  for (int i = tid; i < kWarps * stride; i += kThreads) hist[i] = 0;
+  __syncthreads();
+
+  const int chunk = ((S + kWarps - 1) / kWarps + 31) / 32 * 32;
+  const int beg = warp * chunk;
+  const int end = min(S, beg + chunk);
+  int* h = hist + warp * stride;
+
+  // Pass 1: per-warp histogram.
+  for (int base = beg; base < end; base += 32) {
+    const int s = base + lane;
+    const unsigned active = __ballot_sync(0xffffffffu, s < end);
+    if (s < end) {
+      const int key = slot_key(idx, s, E, status);
+      const unsigned peers = __match_any_sync(active, key);
+      if (lane == __ffs(peers) - 1) h[key] += __popc(peers);
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+
+  // Exclusive prefix over warps for each key; totals per key.
+  int cnt = 0;
+  if (tid <= E) {
+    int run = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = hist[w * stride + tid];
+      hist[w * stride + tid] = run;
+      run += c;
+    }
+    cnt = run;
+  }
+  const int c_e = (tid < E) ? cnt : 0;
+  const int off = block_excl_scan(c_e, warp_sums, &tot[0]);
+  const int pad = block_excl_scan((c_e + kRowAlign - 1) / kRowAlign * kRowAlign, warp_sums, &tot[1]);
+  const int mts = block_excl_scan((c_e + kBlockM - 1) / kBlockM, warp_sums, &tot[2]);
+  if (tid < E) {
+    counts[tid] = c_e;
+    offsets[tid] = off;
+    padded_offsets[tid] = pad;
+    tiles[kTilesHdr + tid] = mts;
+    s_off[tid] = off;
+    s_pad[tid] = pad;
+  }
+  if (tid == 0) {
+    offsets[E] = tot[0];
+    padded_offsets[E] = tot[1];
+    tiles[kTilesHdr + E] = tot[2];
+    tiles[0] = tot[2];
+    s_off[E] = tot[0];
+    s_pad[E] = tot[1];
+  }
+  __syncthreads();
+
+  // Pass 2: scatter.
+  for (int base = beg; base < end; base += 32) {
+    const int s = base + lane;
+    const unsigned active = __ballot_sync(0xffffffffu, s < end);
+    if (s < end) {
+      const int key = slot_key(idx, s, E, status);
+      const unsigned peers = __match_any_sync(active, key);
+      const int leader = __ffs(peers) - 1;
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      const int pos = h[key] + rank;
+      __syncwarp(active);
+      if (lane == leader) h[key] += __popc(peers);
+      perm[s_off[key] + pos] = s;
+      if (key < E) {
+        const int row = s_pad[key] + pos;
+        inv[s] = row;
+        row_slot[row] = s;
+      } else {
+        inv[s] = -1;
+      }
+    }
+    __syncwarp();
+  }
+
+  // Padding rows of every group belong to no slot.
+  for (int e = warp; e < E; e += kWarps) {
+    const int lo = s_pad[e] + (s_off[e + 1] - s_off[e]);
+    const int hi = s_pad[e + 1];
+    for (int r = lo + lane; r < hi; r += 32) row_slot[r] = -1;
+  }
+  (void)M;
+}
+
+}  // namespace
+
+cudaError_t launch_route(const int32_t* topk_idx, int S, int E, const WsLayout& L, uint8_t* ws, cudaStream_t st) {
+  const moe_workspace_layout& p = L.pub;
+  const size_t smem = sizeof(int) * kWarps * (E + 1);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  route_kernel<<<1, kThreads, smem, st>>>(
+      topk_idx, S, E, L.M, reinterpret_cast<int32_t*>(ws + p.counts), reinterpret_cast<int32_t*>(ws + p.offsets),
+      reinterpret_cast<int32_t*>(ws + p.padded_offsets), reinterpret_cast<int32_t*>(ws + p.perm),
+      reinterpret_cast<int32_t*>(ws + p.inv), reinterpret_cast<int32_t*>(ws + p.row_slot),
+      reinterpret_cast<int32_t*>(ws + p.tiles), reinterpret_cast<uint32_t*>(ws + p.status));
+  return cudaGetLastError();
+}
+
+}  // namespace bsmoe

@@ -1,0 +1,192 @@
+/*
+ * Block-scaled MoE experts forward for one GB300 (sm_103a): C ABI.
+ *
+ * The operation is the experts half of a Mixture-of-Experts layer as the
+ * transformers integration pages describe it:
+ *
+ *   - "fp8_grouped_mm_experts_forward" (finegrained_fp8.py error page, source
+ *     excerpt): flatten the T*K token-expert pairs, sort them by expert,
+ *     gather hidden rows by slot // K, run the grouped block-scaled matmuls
+ *     with activations quantized dynamically per block, zero the sentinel
+ *     rows, reduce the top-k rows of each token with a deterministic
+ *     reshape+sum (no atomics) and cast back to the input dtype;
+ *   - "deepgemm_fp8_fp4_experts_forward" (deepgemm.py error record, excerpt
+ *     lines 678-714): grouped FP8-activation x FP8/FP4-weight matmuls over a
+ *     padded grouped layout (sorted_to_padded), bf16 hidden states only,
+ *     static activation scales refused, one CUDA device per call;
+ *   - the DeepGEMM Mega MoE forward docstring (deepgemm.py error page, lines
+ *     857-893): top-k ids are GLOBAL expert ids and -1 marks a skipped slot;
+ *     gate_up / down weights carry UE8M0 scale factors and are transformed
+ *     once before the first forward (scale packing and weight interleave);
+ *     swiglu_limit is an optional clamp, unclamped when absent.
+ *
+ * Formats (fixed here, the pages only name them):
+ *   MOE_W_FP8: e4m3 weight codes with one fp32 scale per 128x128 block
+ *              (weight = code * scale);
+ *   MOE_W_FP4: e2m1 codes packed two per byte along K (low nibble = even K
+ *              index) with one UE8M0 byte per 1x32 block along K
+ *              (weight = code * 2^(byte - 127)).
+ *   Activations (hidden and the SwiGLU output) are quantized per 1x128 block
+ *   to e4m3 with a power-of-two scale 2^e, e = min{n : amax <= 448 * 2^n}.
+ *   SwiGLU: rows [0, I) of w13 are gate, [I, 2I) are up; with a limit L,
+ *   gate = min(gate, L) and up = clamp(up, -L, L); act = silu(gate) * up.
+ *
+ * Conventions for every call:
+ *   - all array pointers are DEVICE pointers on the calling thread's current
+ *     device unless stated otherwise; weights, prepared weights and the
+ *     workspace must be 256-byte aligned, hidden and out 16-byte aligned,
+ *     topk_idx and topk_w 4-byte aligned (MOE_ERR_ALIGNMENT otherwise);
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream); every device
+ *     call is enqueued on it and returns without synchronizing, except
+ *     moe_get_device_status;
+ *   - nothing is allocated: the caller owns every buffer, including the
+ *     workspace, whose size comes from moe_workspace_bytes;
+ *   - a non-MOE_OK status means nothing was enqueued.
+ */
+#ifndef BSMOE_MOE_EXPERTS_H_
+#define BSMOE_MOE_EXPERTS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,        /* null pointer, negative size, T > capacity */
+  MOE_ERR_UNSUPPORTED_SHAPE = 2,  /* dimension outside what the kernels take */
+  MOE_ERR_UNSUPPORTED_ARCH = 3,   /* device is not compute capability 10.3 */
+  MOE_ERR_DEVICE_MISMATCH = 4,    /* a pointer is not memory of the current device */
+  MOE_ERR_ALIGNMENT = 5,          /* a pointer is not 256-byte aligned */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 6,
+  MOE_ERR_CUDA = 7,               /* a CUDA runtime/driver call failed */
+  MOE_ERR_DEVICE_FAULT = 8        /* moe_get_device_status found flags set */
+} moe_status;
+
+typedef enum {
+  MOE_W_FP8 = 0, /* e4m3 + fp32 128x128 block scales */
+  MOE_W_FP4 = 1  /* e2m1 packed in bytes + UE8M0 1x32 block scales */
+} moe_wfmt;
+
+/* Sticky flags in the workspace status word (moe_get_device_status). */
+#define MOE_DEV_BAD_EXPERT_ID 0x1u /* an id outside [-1, E): treated as skipped */
+#define MOE_DEV_TIMEOUT 0x2u       /* a pipeline wait gave up; outputs invalid */
+
+/* Human-readable name of a status code; never NULL. */
+const char* moe_status_string(int status);
+
+/* MOE_ABI_VERSION of the loaded library. */
+int moe_abi_version(void);
+
+/*
+ * Supported shapes: 1 <= E <= 512, 1 <= K <= 32, H and I multiples of 64
+ * (multiples of 128 for MOE_W_FP8, whose weight blocks are 128x128),
+ * 128 <= H, I <= 32768. T may be 0 (nothing is enqueued).
+ */
+
+/*
+ * Bytes of the prepared (kernel-layout) weights made by moe_prepare_weights.
+ * Returns 0 for an unsupported shape or format.
+ */
+size_t moe_prepared_w13_bytes(int fmt, int E, int H, int I);
+size_t moe_prepared_w2_bytes(int fmt, int E, int H, int I);
+
+/*
+ * Bytes of workspace a forward with up to T_max tokens needs. A workspace of
+ * this size serves every call with T <= T_max and the same (fmt, H, I, E, K).
+ * Returns 0 for an unsupported shape.
+ */
+size_t moe_workspace_bytes(int fmt, int T_max, int H, int I, int E, int K);
+
+/*
+ * One-shot weight transform, the analogue of the Mega MoE "pack UE8M0 SFs
+ * and interleave the L1/L2 weights" first-forward step (made explicit here
+ * instead of lazy). Reads the checkpoint-layout weights and writes the
+ * kernel layout: gate/up rows interleaved in 64-row groups, K padded to a
+ * multiple of 128 and N to a multiple of 256 with zeros, scale factors
+ * rearranged into the layout the tensor-core pipeline stages.
+ *
+ * Inputs (read only, device):
+ *   MOE_W_FP8: w13 u8 [E, 2I, H], w13_scale f32 [E, 2I/128, H/128],
+ *              w2  u8 [E, H, I],  w2_scale  f32 [E, H/128, I/128];
+ *   MOE_W_FP4: w13 u8 [E, 2I, H/2], w13_scale u8 [E, 2I, H/32],
+ *              w2  u8 [E, H, I/2],  w2_scale  u8 [E, H, I/32].
+ * Outputs (device, caller-owned): w13_prep of moe_prepared_w13_bytes,
+ *   w2_prep of moe_prepared_w2_bytes. Their content is opaque.
+ * Errors: MOE_ERR_INVALID_ARG / UNSUPPORTED_SHAPE / ALIGNMENT /
+ *   DEVICE_MISMATCH / UNSUPPORTED_ARCH / WORKSPACE_TOO_SMALL (an output
+ *   buffer smaller than required) / CUDA.
+ */
+moe_status moe_prepare_weights(int fmt, int E, int H, int I, const void* w13, const void* w13_scale,
+                               const void* w2, const void* w2_scale, void* w13_prep, size_t w13_prep_bytes,
+                               void* w2_prep, size_t w2_prep_bytes, void* stream);
+
+/*
+ * The experts forward:
+ *   out[t, :] = bf16( sum_{k : idx[t,k] valid} w[t,k] * FFN_{idx[t,k]}(x[t, :]) )
+ * summed in ascending k in fp32 (deterministic, no atomics); a token whose
+ * slots are all skipped gets +0.
+ *
+ *   hidden    bf16 [T, H] (row-major), device
+ *   topk_idx  int32 [T, K] global expert ids, -1 = skipped slot
+ *   topk_w    fp32 [T, K] routing weights (ignored for skipped slots)
+ *   w13_prep, w2_prep  from moe_prepare_weights with the same (fmt, E, H, I)
+ *   swiglu_limit  clamp L; NaN or <= 0 means unclamped
+ *   workspace  >= moe_workspace_bytes(fmt, T, H, I, E, K) bytes, device
+ *   out       bf16 [T, H], device; must not overlap any input
+ *
+ * Ids outside [-1, E) are treated as skipped and set MOE_DEV_BAD_EXPERT_ID.
+ * Asynchronous; the workspace must not be used by another call until this
+ * one has finished on `stream`.
+ */
+moe_status moe_experts_forward(const void* hidden, const int32_t* topk_idx, const float* topk_w, int T, int H,
+                               int I, int E, int K, int fmt, const void* w13_prep, const void* w2_prep,
+                               float swiglu_limit, void* workspace, size_t workspace_bytes, void* out,
+                               void* stream);
+
+/*
+ * Synchronizes `stream` and reads the status word of `workspace` into *flags
+ * (host pointer), then clears it. The word holds the flags raised by the most
+ * recent forward that used this workspace (each forward starts by clearing
+ * it). Returns MOE_ERR_DEVICE_FAULT when a flag was set, MOE_OK otherwise.
+ */
+moe_status moe_get_device_status(void* workspace, void* stream, uint32_t* flags);
+
+/*
+ * Byte offsets of the forward's intermediate results inside the workspace,
+ * for inspection after a forward (tests compare them with the oracle).
+ * All regions are int32 unless noted; M = padded row capacity.
+ *   counts [E]; offsets [E+1] (exclusive scan of counts);
+ *   padded_offsets [E+1] (group starts, multiples of row_align);
+ *   perm [S] (sorted position -> slot, skipped slots last);
+ *   inv [S] (slot -> padded row, -1 if skipped);
+ *   row_slot [M] (padded row -> slot, -1 for padding rows);
+ *   xq u8 [M, xq_cols] (e4m3 hidden rows in grouped order);
+ *   xsf u32 (activation scale words, see below);
+ *   act u8 [M, act_cols] (e4m3 SwiGLU output), asf u32 likewise;
+ *   y f32 [M, H] (weighted per-pair outputs).
+ * Scale words: for row r and 128-column block b the word sits at index
+ *   ((r / 128) * nblk + b) * 128 + 4 * (r % 32) + (r % 128) / 32
+ * and holds the UE8M0 byte (e + 127) replicated in all four bytes.
+ */
+typedef struct {
+  size_t total_bytes;
+  size_t status, counts, offsets, padded_offsets, perm, inv, row_slot, tiles;
+  size_t xq, xsf, act, asf, y;
+  int32_t row_capacity;  /* M */
+  int32_t row_align;     /* group alignment A */
+  int32_t xq_cols, act_cols;
+  int32_t x_blocks, act_blocks; /* ceil(H/128), ceil(I/128) */
+} moe_workspace_layout;
+
+moe_status moe_query_workspace_layout(int fmt, int T, int H, int I, int E, int K, moe_workspace_layout* layout);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSMOE_MOE_EXPERTS_H_ */

@@ -1,0 +1,102 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path, run the oracle
+on the same bytes, compare with the tolerances of the method's statement.
+
+Tolerances (bf16 output vs the fp64 oracle):
+* relative Frobenius error <= 2e-3;
+* elementwise: max(0, |gpu - ref| - ulp_bf16(ref) / 2) <= 1e-2 * RMS(ref).
+  The half-ulp allowance is the reading taken for the max-error bound: the
+  bf16 output alone cannot meet 1e-2 * RMS for |ref| > 2.56 * RMS, so the
+  bound applies to the error beyond the unavoidable final rounding.
+"""
+import numpy as np
+import torch
+
+import oracle.moe as OM
+from oracle import formats as OF
+from block_scaled_moe_expert_gb300 import binding as B
+from block_scaled_moe_expert_gb300 import workloads as W
+
+REL_FRO = 2e-3
+MAX_REL_RMS = 1e-2
+
+
+class LazyExperts:
+    """Indexable by expert: copies one expert's weights to host on demand."""
+
+    def __init__(self, t):
+        self.t = t
+        self.cache = {}
+
+    def __getitem__(self, e):
+        e = int(e)
+        if e not in self.cache:
+            self.cache = {e: self.t[e].cpu().numpy()}
+        return self.cache[e]
+
+
+def oracle_weights(weights):
+    return dict(fmt=weights["fmt"], E=weights["E"], H=weights["H"], I=weights["I"],
+                w13=LazyExperts(weights["w13"]), w13_scale=LazyExperts(weights["w13_scale"]),
+                w2=LazyExperts(weights["w2"]), w2_scale=LazyExperts(weights["w2_scale"]))
+
+
+def bits_of(hidden):
+    return hidden.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def oracle_out(hidden, idx, w, weights, limit, tokens=None):
+    return OM.experts_forward(bits_of(hidden), idx.cpu().numpy(), w.cpu().numpy(), oracle_weights(weights),
+                              limit, tokens=tokens)
+
+
+def compare(gpu_bf16, ref):
+    g = gpu_bf16.float().cpu().numpy().astype(np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    nrm = float(np.linalg.norm(ref))
+    rel = float(np.linalg.norm(g - ref) / nrm) if nrm > 0 else float(np.abs(g).max())
+    _, E = np.frexp(ref)
+    half_ulp = np.ldexp(1.0, np.maximum(E - 8, -133)) / 2
+    excess = np.maximum(np.abs(g - ref) - half_ulp, 0.0)
+    raw = float(np.abs(g - ref).max()) if g.size else 0.0
+    return dict(rel_fro=rel, max_excess_over_rms=float(excess.max() / rms) if rms > 0 else float(excess.max()),
+                max_raw_over_rms=raw / rms if rms > 0 else raw, rms=rms, finite=bool(np.isfinite(g).all()))
+
+
+def assert_close(gpu_bf16, ref, what=""):
+    m = compare(gpu_bf16, ref)
+    assert m["finite"], (what, m)
+    assert m["rel_fro"] <= REL_FRO, (what, m)
+    assert m["max_excess_over_rms"] <= MAX_REL_RMS, (what, m)
+    return m
+
+
+def run_cuda(wl, device="cuda", hidden=None, idx=None, w=None, weights=None, prepared=None):
+    hidden = W.make_hidden(wl, device) if hidden is None else hidden
+    if idx is None:
+        idx, w = W.make_routing(wl, device)
+    weights = W.make_weights(wl, device) if weights is None else weights
+    prepared = B.prepare_weights(weights) if prepared is None else prepared
+    ws = torch.empty(B.workspace_bytes(wl.fmt, wl.T, wl.H, wl.I, wl.E, wl.K), dtype=torch.uint8, device=device)
+    out = B.experts_forward(hidden, idx, w, prepared, wl.swiglu_limit, workspace=ws)
+    torch.cuda.synchronize()
+    return dict(hidden=hidden, idx=idx, w=w, weights=weights, prepared=prepared, ws=ws, out=out)
+
+
+def ws_region(ws, layout, name, dtype, count):
+    off = getattr(layout, name)
+    nbytes = count * torch.empty(0, dtype=dtype).element_size()
+    return ws[off:off + nbytes].view(dtype)
+
+
+def sf_exponents(words_u32, rows, nblk):
+    """Read the per-(row, block) exponents out of the scale-word layout."""
+    w = words_u32.cpu().numpy().astype(np.int64)
+    r = np.arange(rows)[:, None]
+    b = np.arange(nblk)[None, :]
+    idx = ((r // 128) * nblk + b) * 128 + 4 * (r % 32) + (r % 128) // 32
+    return (w[idx] & 0xFF) - 127
+
+
+__all__ = ["oracle_out", "compare", "assert_close", "run_cuda", "ws_region", "sf_exponents", "bits_of", "OF",
+           "OM", "W", "B"]

@@ -1,0 +1,116 @@
+"""GPU: the experts forward through the C ABI against the fp64 oracle.
+
+Sizes the oracle finishes in seconds that still span several m and n tiles
+with ragged tails, in both weight formats, plus the degenerate cases.
+"""
+import numpy as np
+import pytest
+import torch
+
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+W = P.W
+
+CASES = [
+    W.WORKLOADS["tiny_fp8"],
+    W.Workload("fp8_ragged", 300, 512, 384, 4, 2, "fp8", "softmax", seed=11),
+    W.Workload("fp8_ragged_clamp", 300, 512, 384, 4, 2, "fp8", "softmax", seed=12, swiglu_limit=0.3),
+    W.Workload("fp8_zipf_skips", 200, 256, 256, 32, 8, "fp8", "zipf_sigmoid", seed=13, skip_frac=0.05),
+    W.Workload("fp4_small", 64, 256, 128, 8, 2, "fp4", "softmax", seed=14),
+    W.Workload("fp4_gptoss_like", 300, 2880, 2880, 8, 4, "fp4", "softmax", seed=15, logit_std=1.5,
+               swiglu_limit=7.0),
+    W.Workload("fp4_ragged_h", 130, 320, 192, 5, 3, "fp4", "softmax", seed=16, swiglu_limit=0.2),
+]
+
+
+@pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
+def test_forward_matches_oracle(wl):
+    r = P.run_cuda(wl)
+    ref = P.oracle_out(r["hidden"], r["idx"], r["w"], r["weights"], wl.swiglu_limit)
+    m = P.assert_close(r["out"], ref, wl.name)
+    assert P.B.device_status(r["ws"]) == 0
+    print(wl.name, m)
+
+
+def test_deterministic_and_batch_invariant():
+    wl = CASES[1]
+    r = P.run_cuda(wl)
+    again = P.B.experts_forward(r["hidden"], r["idx"], r["w"], r["prepared"], wl.swiglu_limit)
+    assert torch.equal(again.view(torch.int16), r["out"].view(torch.int16))
+    # Appending all-skipped tokens (the padded last slice of the shared-batch
+    # example) changes no bit of the real tokens and gives +0 rows.
+    pad = 37
+    hid = torch.cat([r["hidden"], r["hidden"][:pad]])
+    idx = torch.cat([r["idx"], torch.full((pad, wl.K), -1, dtype=torch.int32, device="cuda")])
+    w = torch.cat([r["w"], r["w"][:pad]])
+    out = P.B.experts_forward(hid, idx, w, r["prepared"], wl.swiglu_limit)
+    assert torch.equal(out[:wl.T].view(torch.int16), r["out"].view(torch.int16))
+    assert (out[wl.T:].view(torch.int16) == 0).all()
+
+
+def test_all_skipped_gives_positive_zero():
+    wl = W.scaled(CASES[1], T=50)
+    idx = torch.full((wl.T, wl.K), -1, dtype=torch.int32, device="cuda")
+    w = torch.rand(wl.T, wl.K, device="cuda")
+    r = P.run_cuda(wl, idx=idx, w=w)
+    assert (r["out"].view(torch.int16) == 0).all()
+
+
+def test_nan_weight_in_skipped_slot_is_never_read():
+    wl = CASES[1]
+    r = P.run_cuda(wl)
+    idx = r["idx"].clone()
+    w = r["w"].clone()
+    idx[5, 0] = -1
+    idx[17, 1] = -1
+    a = P.B.experts_forward(r["hidden"], idx, w, r["prepared"])
+    w[5, 0] = float("nan")
+    w[17, 1] = float("inf")
+    b = P.B.experts_forward(r["hidden"], idx, w, r["prepared"])
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    ref = P.oracle_out(r["hidden"], idx, w, r["weights"], None)
+    P.assert_close(b, ref, "nan weights")
+
+
+@pytest.mark.parametrize("T", [1, 2, 127, 129])
+def test_small_token_counts(T):
+    wl = W.Workload("fp8_small_T", T, 256, 256, 6, 2, "fp8", "softmax", seed=20 + T)
+    r = P.run_cuda(wl)
+    P.assert_close(r["out"], P.oracle_out(r["hidden"], r["idx"], r["w"], r["weights"], None), f"T={T}")
+
+
+def test_single_expert_top1():
+    wl = W.Workload("e1k1", 200, 256, 128, 1, 1, "fp8", "softmax", seed=31)
+    r = P.run_cuda(wl)
+    P.assert_close(r["out"], P.oracle_out(r["hidden"], r["idx"], r["w"], r["weights"], None), "E=1,K=1")
+
+
+def test_zero_tokens_enqueues_nothing():
+    wl = CASES[0]
+    weights = W.make_weights(wl, "cuda")
+    prepared = P.B.prepare_weights(weights)
+    hid = torch.empty(0, wl.H, dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty(0, wl.K, dtype=torch.int32, device="cuda")
+    w = torch.empty(0, wl.K, dtype=torch.float32, device="cuda")
+    out = P.B.experts_forward(hid, idx, w, prepared)
+    assert out.shape == (0, wl.H)
+
+
+def test_refusals():
+    wl = CASES[0]
+    r = P.run_cuda(wl)
+    with pytest.raises(ValueError):
+        P.B.experts_forward(r["hidden"].float(), r["idx"], r["w"], r["prepared"])
+    with pytest.raises(NotImplementedError):
+        P.B.experts_forward(r["hidden"], r["idx"], r["w"], r["prepared"], activation_scheme="static")
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(P.B.MoeError):
+        P.B.experts_forward(r["hidden"], r["idx"], r["w"], r["prepared"], workspace=small)
+    host = r["hidden"].cpu()
+    L = P.B.lib()
+    st = L.moe_experts_forward(host.data_ptr(), r["idx"].data_ptr(), r["w"].data_ptr(), wl.T, wl.H, wl.I, wl.E,
+                               wl.K, 0, r["prepared"].w13_prep.data_ptr(), r["prepared"].w2_prep.data_ptr(),
+                               float("nan"), r["ws"].data_ptr(), r["ws"].numel(), r["out"].data_ptr(), None)
+    assert st == 4  # MOE_ERR_DEVICE_MISMATCH: a host pointer
