@@ -1,0 +1,372 @@
+#!/usr/bin/env python
+"""Benchmark of the block-scaled MoE experts forward on GB300.
+
+One step = one moe_experts_forward (routing, input quantization, GEMM1 with
+the SwiGLU epilogue, GEMM2, combine) over the workload's synthetic batch with
+every input resident in HBM. Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Metric: algorithmic TFLOP/s (6 * H * I * pairs per step; padding rows are not
+counted) and tokens/s of the experts forward on one GB300. The default
+workload is the Mixtral-8x7B-shaped FP8 prefill layer (T=4096, H=4096,
+I=14336, E=8, K=2). Multi-GPU runs are independent replicas (weak scaling):
+the forward has no exchange step on one GPU.
+
+Legs in the line: `value` (device time, inputs already in HBM), `e2e` (the
+same metric through the C ABI with pinned host buffers, copies inside the
+timed region), `roofline` (the dominant kernel timed with CUDA events on the
+launching stream against the measured peak), `cpu_baseline` (the fp64 oracle
+on the host cores over a bounded sample), `clocks` (nvidia-smi sampled during
+the timed region). `--impl reference` times the oracle alone on the host
+cores, on the same workload and metric.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE experts fwd TFLOPS + tokens/s; % of FP8/FP4 TC peak or HBM BW (1 GB300)"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+STAGES = ["route", "quant", "gemm1", "gemm2", "combine"]
+TC_BOUND = {"mixtral_prefill_fp8", "gptoss_fp8xfp4", "dsv3_prefill_fp8", "tiny_fp8"}
+CPU_SAMPLE_TOKENS = {"mixtral_prefill_fp8": 4, "dsv3_prefill_fp8": 3, "dsv3_decode_fp8": 3, "gptoss_fp8xfp4": 24}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def weight_bytes_per_expert(wl, which):
+    """Algorithmic bytes of one expert's weight (codes + scales)."""
+    rows, k = (2 * wl.I, wl.H) if which == 13 else (wl.H, wl.I)
+    if wl.fmt == "fp8":
+        return rows * k + 4 * ((rows + 127) // 128) * ((k + 127) // 128)
+    return rows * k // 2 + rows * (k // 32)
+
+
+def routing_stats(idx_cpu, E):
+    ids = idx_cpu.reshape(-1)
+    valid = ids[(ids >= 0) & (ids < E)]
+    return int(valid.size), int(np.unique(valid).size)
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while it runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.dev = device_index
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                                       "--format=csv,noheader,nounits", "-lms", "20"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.p = None
+        return self
+
+    def __exit__(self, *a):
+        if self.p is not None:
+            time.sleep(0.1)
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+
+    def summary(self, t0, t1):
+        self.f.flush()
+        rows = []
+        with open(self.f.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) == 8:
+                    rows.append(parts)
+        os.unlink(self.f.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        # under load: samples at the top of the observed power range
+        pw = [num(r[2]) or 0.0 for r in rows]
+        thr = max(pw) * 0.5 if pw else 0
+        loaded = [num(r[0]) for r, p in zip(rows, pw) if p >= thr and num(r[0]) is not None] or sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[4:8]) if v.strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": num(rows[0][1]), "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+def cpu_baseline(wl, hidden, idx, w, weights, n_tok):
+    """Time the oracle (as it stands) on the first n_tok tokens."""
+    import torch
+    from oracle import moe as OM
+
+    class Lazy:
+        def __init__(self, t):
+            self.t, self.k, self.v = t, None, None
+
+        def __getitem__(self, e):
+            if self.k != int(e):
+                self.k, self.v = int(e), self.t[int(e)].cpu().numpy()
+            return self.v
+
+    wts = dict(fmt=wl.fmt, E=wl.E, H=wl.H, I=wl.I, **{k: Lazy(weights[k]) for k in
+                                                        ("w13", "w13_scale", "w2", "w2_scale")})
+    toks = np.arange(min(n_tok, wl.T))
+    bits = hidden[:len(toks)].view(torch.int16).cpu().numpy().view(np.uint16)
+    ids = idx[:len(toks)].cpu().numpy()
+    ws = w[:len(toks)].cpu().numpy()
+    bits_full = np.zeros((len(toks), wl.H), np.uint16)
+    bits_full[:] = bits
+    t0 = time.perf_counter()
+    OM.experts_forward(bits_full, ids, ws, wts, wl.swiglu_limit)
+    dt = time.perf_counter() - t0
+    pairs, _ = routing_stats(ids, wl.E)
+    cores = len(os.sched_getaffinity(0))
+    return {"value": 6.0 * wl.H * wl.I * pairs / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"first {len(toks)} tokens ({pairs} pairs) of {wl.name}, fp64 numpy, {dt:.1f} s",
+            "tokens_per_s": len(toks) / dt}
+
+
+def run_reference(args, wl):
+    """Reference arm: the fp64 oracle on the host cores, per step one token."""
+    import torch
+    from block_scaled_moe_expert_gb300 import workloads as W
+    from oracle import moe as OM
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    small = W.scaled(wl, T=min(wl.T, 64))
+    hidden = W.make_hidden(small)
+    idx, w = W.make_routing(small)
+    # One expert's worth of synthetic weights (same shapes and distribution)
+    # stands in for every expert: the oracle's cost does not depend on the
+    # values, and drawing all E experts on the host would dominate the run.
+    touched = sorted({int(e) for e in idx.reshape(-1).tolist() if 0 <= e < wl.E})
+    one = W.make_weights(W.scaled(wl, E=1), "cpu")
+    one = {k: one[k][0].numpy() for k in ("w13", "w13_scale", "w2", "w2_scale")}
+
+    class Gen:
+        def __init__(self, key):
+            self.key = key
+
+        def __getitem__(self, e):
+            return one[self.key]
+
+    wts = dict(fmt=wl.fmt, E=wl.E, H=wl.H, I=wl.I, **{k: Gen(k) for k in ("w13", "w13_scale", "w2", "w2_scale")})
+    bits = hidden.view(torch.int16).numpy().view(np.uint16)
+    ids = idx.numpy()
+    wv = w.numpy()
+    times, pairs = [], []
+    for step in range(args.warmup + args.steps):
+        t = step % small.T
+        t0 = time.perf_counter()
+        OM.experts_forward(bits, ids, wv, wts, wl.swiglu_limit, tokens=[t])
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            times.append(dt)
+            pairs.append(routing_stats(ids[t:t + 1], wl.E)[0])
+    total = sum(times)
+    flops = 6.0 * wl.H * wl.I * sum(pairs)
+    value = flops / total / 1e12
+    cores = len(os.sched_getaffinity(0))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
+                                            "K": wl.K, "weights": wl.fmt},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"one token of {wl.name} per step (synthetic expert weights), fp64 numpy"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "tokens_per_s": args.steps / total, "touched_experts_sample": len(touched)}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, wl):
+    import torch
+    from block_scaled_moe_expert_gb300 import binding as B
+    from block_scaled_moe_expert_gb300 import build as BLD
+    from block_scaled_moe_expert_gb300 import workloads as W
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    BLD.build()
+    dev = torch.device("cuda", local)
+    hidden, idx, w, weights = W.make_all(wl, dev)
+    prepared = B.prepare_weights(weights)
+    ws = torch.empty(B.workspace_bytes(wl.fmt, wl.T, wl.H, wl.I, wl.E, wl.K), dtype=torch.uint8, device=dev)
+    out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
+    pairs, touched = routing_stats(idx.cpu().numpy(), wl.E)
+    flops = 6.0 * wl.H * wl.I * pairs
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    def new_events(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in evs:
+            e.record()
+        return evs
+
+    for _ in range(args.warmup):
+        B.experts_forward(hidden, idx, w, prepared, wl.swiglu_limit, workspace=ws, out=out)
+    torch.cuda.synchronize()
+    if B.device_status(ws) != 0:
+        raise RuntimeError("device status flags set during warm-up")
+
+    stage_ev = [new_events(6) for _ in range(args.steps)]
+    start, stop = new_events(2)
+    torch.cuda.synchronize()
+    peaks, peak_src = load_peaks()
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        t_wall0 = time.time()
+        start.record()
+        for s in range(args.steps):
+            B.experts_forward_timed(hidden, idx, w, prepared, stage_ev[s], wl.swiglu_limit, workspace=ws, out=out)
+        stop.record()
+        torch.cuda.synchronize()
+        barrier()
+        t_wall1 = time.time()
+    clocks = clk.summary(t_wall0, t_wall1)
+    total_ms = start.elapsed_time(stop)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    stage_ms = {name: statistics.fmean(ev[i].elapsed_time(ev[i + 1]) for ev in stage_ev)
+                for i, name in enumerate(STAGES)}
+    status = B.device_status(ws)
+
+    # e2e: pinned host inputs, copies and the result read-back inside the region
+    e2e = None
+    if not args.no_e2e:
+        h_hidden = hidden.cpu().pin_memory()
+        h_idx = idx.cpu().pin_memory()
+        h_w = w.cpu().pin_memory()
+        h_out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16).pin_memory()
+        d_hidden, d_idx, d_w = torch.empty_like(hidden), torch.empty_like(idx), torch.empty_like(w)
+        e0, e1 = new_events(2)
+        torch.cuda.synchronize()
+        barrier()
+        e0.record()
+        for _ in range(args.steps):
+            d_hidden.copy_(h_hidden, non_blocking=True)
+            d_idx.copy_(h_idx, non_blocking=True)
+            d_w.copy_(h_w, non_blocking=True)
+            B.experts_forward(d_hidden, d_idx, d_w, prepared, wl.swiglu_limit, workspace=ws, out=out)
+            h_out.copy_(out, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / args.steps
+        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": hidden.numel() * 2 + idx.numel() * 4 + w.numel() * 4,
+               "d2h_bytes_per_step": out.numel() * 2, "ms_per_step": e2e_ms}
+
+    # Roofline of the dominant kernel.
+    dom = max(("gemm1", "gemm2"), key=lambda k: stage_ms[k])
+    frac_1 = 2.0 / 3.0 if dom == "gemm1" else 1.0 / 3.0
+    if wl.name in TC_BOUND:
+        peak = 2.0 * peaks["bf16_tflops"]  # fp8 dense = 2 x bf16 dense (nominal 4.5 / 2.25 PF)
+        achieved = flops * frac_1 / (stage_ms[dom] * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"{peak_src}: 2 x bf16 burst (fp8/bf16 nominal ratio 2)"}
+        alg_units = f"{frac_1:.3f} x 6*H*I*pairs flops"
+    else:
+        wb = weight_bytes_per_expert(wl, 13 if dom == "gemm1" else 2) * touched
+        if dom == "gemm1":
+            act = pairs * (wl.H + 4 * ((wl.H + 127) // 128)) + pairs * (wl.I + 4 * ((wl.I + 127) // 128))
+        else:
+            act = pairs * (wl.I + 4 * ((wl.I + 127) // 128)) + pairs * wl.H * 4
+        achieved = (wb + act) / (stage_ms[dom] * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_source": f"{peak_src}: copy bandwidth"}
+        alg_units = "touched-expert weight bytes + activation bytes"
+    roof.update({"kernel": dom, "traffic": None, "kernel_ms": stage_ms[dom], "algorithmic": alg_units})
+
+    line = {"metric": METRIC, "value": world * flops / (ms_step * 1e-3) / 1e12, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if wl.fmt == "fp8" else "e4m3xe2m1",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "K": wl.K,
+                       "weights": wl.fmt, "swiglu_limit": wl.swiglu_limit, "pairs": pairs,
+                       "touched_experts": touched, "parallelism": f"replicas{world}",
+                       "l2": "inputs larger than L2 (expert weights stream from HBM every step)"},
+            "tokens_per_s": world * wl.T / (ms_step * 1e-3),
+            "stage_ms": stage_ms, "roofline": roof, "gpu_launches": 5 * args.steps, "clocks": clocks,
+            "device_status": status}
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, hidden, idx, w, weights,
+                                            args.cpu_tokens or CPU_SAMPLE_TOKENS.get(wl.name, 4))
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mixtral_prefill_fp8")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    from block_scaled_moe_expert_gb300 import workloads as W
+    wl = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

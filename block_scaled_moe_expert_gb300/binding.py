@@ -48,6 +48,8 @@ _SIGS = {
     "moe_prepare_weights": (_int, [_int, _int, _int, _int, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _sz, _vp]),
     "moe_experts_forward": (_int, [_vp, _vp, _vp, _int, _int, _int, _int, _int, _int, _vp, _vp, _f32, _vp, _sz,
                                    _vp, _vp]),
+    "moe_experts_forward_timed": (_int, [_vp, _vp, _vp, _int, _int, _int, _int, _int, _int, _vp, _vp, _f32, _vp,
+                                         _sz, _vp, _vp, _c.POINTER(_vp)]),
     "moe_get_device_status": (_int, [_vp, _vp, _c.POINTER(_c.c_uint32)]),
     "moe_query_workspace_layout": (_int, [_int, _int, _int, _int, _int, _int, _c.POINTER(MoeLayout)]),
 }
@@ -164,6 +166,26 @@ def experts_forward(hidden, topk_idx, topk_w, prepared, swiglu_limit=None, works
     return out
 
 
+def experts_forward_timed(hidden, topk_idx, topk_w, prepared, events, swiglu_limit=None, workspace=None,
+                          out=None):
+    """experts_forward that records 6 torch.cuda.Event objects at the stage
+    boundaries (before routing, after routing, quantization, GEMM1, GEMM2,
+    combine) on the current stream."""
+    T, H = hidden.shape
+    K = topk_idx.shape[1]
+    p = prepared
+    if workspace is None:
+        workspace = torch.empty(workspace_bytes(p.fmt, T, H, p.I, p.E, K), dtype=torch.uint8, device=hidden.device)
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=hidden.device)
+    ev = (_vp * 6)(*[_vp(e.cuda_event) for e in events])
+    limit = float("nan") if swiglu_limit is None else float(swiglu_limit)
+    _check(lib().moe_experts_forward_timed(_ptr(hidden), _ptr(topk_idx), _ptr(topk_w), T, H, p.I, p.E, K,
+                                           FMT[p.fmt], _ptr(p.w13_prep), _ptr(p.w2_prep), limit, _ptr(workspace),
+                                           workspace.numel(), _ptr(out), _stream(), ev), "moe_experts_forward_timed")
+    return out
+
+
 def device_status(workspace):
     """Synchronize and return the forward's device flags (0 if clean)."""
     flags = _c.c_uint32(0)
@@ -179,5 +201,5 @@ def header_symbols():
     return sorted(set(re.findall(r"^\w[\w\s\*]*?\b(moe_\w+)\s*\(", src, flags=re.M)))
 
 
-__all__ = ["lib", "MoeError", "prepare_weights", "experts_forward", "workspace_bytes", "workspace_layout",
+__all__ = ["lib", "MoeError", "prepare_weights", "experts_forward", "experts_forward_timed", "workspace_bytes", "workspace_layout",
            "device_status", "PreparedWeights", "header_symbols", "MOE_DEV_BAD_EXPERT_ID", "MOE_DEV_TIMEOUT"]

@@ -213,10 +213,12 @@ moe_status moe_prepare_weights(int fmt, int E, int H, int I, const void* w13, co
   return MOE_OK;
 }
 
-moe_status moe_experts_forward(const void* hidden, const int32_t* topk_idx, const float* topk_w, int T, int H,
+}  // extern "C"
+
+static moe_status forward_impl(const void* hidden, const int32_t* topk_idx, const float* topk_w, int T, int H,
                                int I, int E, int K, int fmt, const void* w13_prep, const void* w2_prep,
                                float swiglu_limit, void* workspace, size_t workspace_bytes, void* out,
-                               void* stream) {
+                               void* stream, void* const* events) {
   if (T < 0 || K < 1 || K > kMaxTopK) return MOE_ERR_INVALID_ARG;
   if (!shape_ok(fmt, H, I, E)) return MOE_ERR_UNSUPPORTED_SHAPE;
   WsLayout L;
@@ -258,8 +260,13 @@ moe_status moe_experts_forward(const void* hidden, const int32_t* topk_idx, cons
                  static_cast<uint64_t>(E) * g2.Np, kBlockN))
     return MOE_ERR_CUDA;
 
-  if (launch_route(topk_idx, L.S, E, L, ws, st) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_quant(hidden, T, H, K, L, ws, st) != cudaSuccess) return MOE_ERR_CUDA;
+  auto mark = [&](int i) {
+    return events == nullptr || events[i] == nullptr ||
+           cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) == cudaSuccess;
+  };
+  if (!mark(0)) return MOE_ERR_CUDA;
+  if (launch_route(topk_idx, L.S, E, L, ws, st) != cudaSuccess || !mark(1)) return MOE_ERR_CUDA;
+  if (launch_quant(hidden, T, H, K, L, ws, st) != cudaSuccess || !mark(2)) return MOE_ERR_CUDA;
 
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -282,7 +289,7 @@ moe_status moe_experts_forward(const void* hidden, const int32_t* topk_idx, cons
   a1.out_cols = g2.Kp;
   a1.out_blocks = g2.KB;
   a1.g = g1;
-  if (launch_gemm(fmt, true, ta1, tb1, a1, d.sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gemm(fmt, true, ta1, tb1, a1, d.sms, st) != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;
 
   GemmArgs a2 = a;
   a2.a_sf = ws + p.asf;
@@ -290,13 +297,35 @@ moe_status moe_experts_forward(const void* hidden, const int32_t* topk_idx, cons
   a2.out_y = reinterpret_cast<float*>(ws + p.y);
   a2.out_cols = H;
   a2.g = g2;
-  if (launch_gemm(fmt, false, ta2, tb2, a2, d.sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gemm(fmt, false, ta2, tb2, a2, d.sms, st) != cudaSuccess || !mark(4)) return MOE_ERR_CUDA;
 
   if (launch_combine(reinterpret_cast<const float*>(ws + p.y), reinterpret_cast<const int32_t*>(ws + p.inv), T, H,
-                     K, out, st) != cudaSuccess)
+                     K, out, st) != cudaSuccess || !mark(5))
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
+
+extern "C" {
+
+moe_status moe_experts_forward(const void* hidden, const int32_t* topk_idx, const float* topk_w, int T, int H,
+                               int I, int E, int K, int fmt, const void* w13_prep, const void* w2_prep,
+                               float swiglu_limit, void* workspace, size_t workspace_bytes, void* out,
+                               void* stream) {
+  return forward_impl(hidden, topk_idx, topk_w, T, H, I, E, K, fmt, w13_prep, w2_prep, swiglu_limit, workspace,
+                      workspace_bytes, out, stream, nullptr);
+}
+
+moe_status moe_experts_forward_timed(const void* hidden, const int32_t* topk_idx, const float* topk_w, int T,
+                                     int H, int I, int E, int K, int fmt, const void* w13_prep,
+                                     const void* w2_prep, float swiglu_limit, void* workspace,
+                                     size_t workspace_bytes, void* out, void* stream, void* const* events) {
+  return forward_impl(hidden, topk_idx, topk_w, T, H, I, E, K, fmt, w13_prep, w2_prep, swiglu_limit, workspace,
+                      workspace_bytes, out, stream, events);
+}
+
+}  // extern "C"
+
+extern "C" {
 
 moe_status moe_get_device_status(void* workspace, void* stream, uint32_t* flags) {
   if (workspace == nullptr || flags == nullptr) return MOE_ERR_INVALID_ARG;

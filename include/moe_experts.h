@@ -149,6 +149,19 @@ moe_status moe_experts_forward(const void* hidden, const int32_t* topk_idx, cons
                                void* stream);
 
 /*
+ * The same forward, doing the same work, that also records events[i]
+ * (cudaEvent_t values created by the caller; a NULL entry is skipped) on
+ * `stream` at the stage boundaries: 0 before routing, 1 after routing,
+ * 2 after the input quantization, 3 after GEMM1 (+SwiGLU epilogue),
+ * 4 after GEMM2, 5 after the combine. `events` points to 6 entries (host
+ * memory). Meant for measuring the stages; errors as moe_experts_forward.
+ */
+moe_status moe_experts_forward_timed(const void* hidden, const int32_t* topk_idx, const float* topk_w, int T,
+                                     int H, int I, int E, int K, int fmt, const void* w13_prep,
+                                     const void* w2_prep, float swiglu_limit, void* workspace,
+                                     size_t workspace_bytes, void* out, void* stream, void* const* events);
+
+/*
  * Synchronizes `stream` and reads the status word of `workspace` into *flags
  * (host pointer), then clears it. The word holds the flags raised by the most
  * recent forward that used this workspace (each forward starts by clearing
