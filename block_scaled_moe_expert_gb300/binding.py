@@ -50,6 +50,9 @@ _SIGS = {
                                    _vp, _vp]),
     "moe_experts_forward_timed": (_int, [_vp, _vp, _vp, _int, _int, _int, _int, _int, _int, _vp, _vp, _f32, _vp,
                                          _sz, _vp, _vp, _c.POINTER(_vp)]),
+    "moe_experts_forward_static": (_int, [_vp, _vp, _vp, _int, _int, _int, _int, _int, _int, _vp, _vp, _f32,
+                                          _vp, _vp]),
+    "moe_static_workspace_capacity": (_sz, []),
     "moe_get_device_status": (_int, [_vp, _vp, _c.POINTER(_c.c_uint32)]),
     "moe_query_workspace_layout": (_int, [_int, _int, _int, _int, _int, _int, _c.POINTER(MoeLayout)]),
 }
@@ -186,6 +189,26 @@ def experts_forward_timed(hidden, topk_idx, topk_w, prepared, events, swiglu_lim
     return out
 
 
+def experts_forward_static(hidden, topk_idx, topk_w, prepared, swiglu_limit=None, out=None):
+    """experts_forward without a workspace: the library's fixed device array
+    (moe_static_workspace_capacity() bytes) is the scratch memory, for
+    callers that cannot allocate. Calls on one device must not overlap."""
+    if hidden.dtype != torch.bfloat16:
+        raise ValueError(f"the experts forward requires bfloat16 hidden states, got {hidden.dtype}")
+    T, H = hidden.shape
+    K = topk_idx.shape[1]
+    p = prepared
+    hidden, topk_idx, topk_w = hidden.contiguous(), topk_idx.contiguous(), topk_w.contiguous()
+    _same_device(hidden, topk_idx, topk_w, p.w13_prep, p.w2_prep)
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=hidden.device)
+    limit = float("nan") if swiglu_limit is None else float(swiglu_limit)
+    _check(lib().moe_experts_forward_static(_ptr(hidden), _ptr(topk_idx), _ptr(topk_w), T, H, p.I, p.E, K,
+                                            FMT[p.fmt], _ptr(p.w13_prep), _ptr(p.w2_prep), limit, _ptr(out),
+                                            _stream()), "moe_experts_forward_static")
+    return out
+
+
 def device_status(workspace):
     """Synchronize and return the forward's device flags (0 if clean)."""
     flags = _c.c_uint32(0)
@@ -201,5 +224,6 @@ def header_symbols():
     return sorted(set(re.findall(r"^\w[\w\s\*]*?\b(moe_\w+)\s*\(", src, flags=re.M)))
 
 
-__all__ = ["lib", "MoeError", "prepare_weights", "experts_forward", "experts_forward_timed", "workspace_bytes", "workspace_layout",
+__all__ = ["lib", "MoeError", "prepare_weights", "experts_forward", "experts_forward_timed", "experts_forward_static",
+           "workspace_bytes", "workspace_layout",
            "device_status", "PreparedWeights", "header_symbols", "MOE_DEV_BAD_EXPERT_ID", "MOE_DEV_TIMEOUT"]

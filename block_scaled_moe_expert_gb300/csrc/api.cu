@@ -215,7 +215,7 @@ moe_status moe_prepare_weights(int fmt, int E, int H, int I, const void* w13, co
 
 }  // extern "C"
 
-static moe_status forward_impl(const void* hidden, const int32_t* topk_idx, const float* topk_w, int T, int H,
+moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, const float* topk_w, int T, int H,
                                int I, int E, int K, int fmt, const void* w13_prep, const void* w2_prep,
                                float swiglu_limit, void* workspace, size_t workspace_bytes, void* out,
                                void* stream, void* const* events) {

@@ -78,6 +78,12 @@ struct GemmArgs {
   GemmGeom g;
 };
 
+// The whole forward on a caller-provided workspace; events (6 entries or
+// null) are recorded at the stage boundaries.
+moe_status forward_impl(const void* hidden, const int32_t* topk_idx, const float* topk_w, int T, int H, int I,
+                        int E, int K, int fmt, const void* w13_prep, const void* w2_prep, float swiglu_limit,
+                        void* workspace, size_t workspace_bytes, void* out, void* stream, void* const* events);
+
 cudaError_t launch_gemm(int fmt, bool is_gemm1, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                         const GemmArgs& args, int num_sms, cudaStream_t st);
 

@@ -162,6 +162,38 @@ moe_status moe_experts_forward_timed(const void* hidden, const int32_t* topk_idx
                                      size_t workspace_bytes, void* out, void* stream, void* const* events);
 
 /*
+ * The forward for callers that cannot allocate device memory (for example a
+ * host runtime that owns every device allocation and only lends out model
+ * tensors, or code running where allocation is not allowed). It takes no
+ * workspace: its scratch memory is one fixed device array inside this
+ * library, moe_static_workspace_capacity() bytes (64 MiB) on every GPU that
+ * loads the library, held until the process exits. The transformers pages
+ * have no counterpart of this call; it exists for such callers only.
+ *
+ * Arguments and results are those of moe_experts_forward minus the
+ * workspace. A call whose moe_workspace_bytes(fmt, T, H, I, E, K) exceeds the
+ * capacity returns MOE_ERR_WORKSPACE_TOO_SMALL and enqueues nothing (at the
+ * DeepSeek-V3 shape, for instance, single-token decode fits and large
+ * batches do not). No cudaMalloc, cudaFree or other allocating routine is
+ * called.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before capturing a stream. Every call shares the one array, and its content
+ * is whatever the last call left there: the forward writes every part it
+ * reads before reading it, so nothing needs clearing, but calls that overlap
+ * on the GPU (other streams, other host threads) race on it and must be
+ * serialized by the caller. The status word of the array is not readable
+ * through moe_get_device_status.
+ */
+moe_status moe_experts_forward_static(const void* hidden, const int32_t* topk_idx, const float* topk_w, int T,
+                                      int H, int I, int E, int K, int fmt, const void* w13_prep,
+                                      const void* w2_prep, float swiglu_limit, void* out, void* stream);
+
+/* Bytes of the fixed device array used by moe_experts_forward_static. */
+size_t moe_static_workspace_capacity(void);
+
+/*
  * Synchronizes `stream` and reads the status word of `workspace` into *flags
  * (host pointer), then clears it. The word holds the flags raised by the most
  * recent forward that used this workspace (each forward starts by clearing
