@@ -357,11 +357,14 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=0)
+    ap.add_argument("--tokens", type=int, default=0, help="override T (smaller profiling cases)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     from block_scaled_moe_expert_gb300 import workloads as W
     wl = W.WORKLOADS[args.workload]
+    if args.tokens:
+        wl = W.scaled(wl, T=args.tokens)
     if args.impl == "reference":
         run_reference(args, wl)
     else:

@@ -15,11 +15,14 @@
 // GEMM2 (A = act, W = down_proj) multiplies each row by the routing weight of
 // its slot and stores fp32 rows for the deterministic combine.
 //
-// Pipeline (one persistent CTA per SM, 10 warps):
+// Pipeline (one persistent CTA per SM, 12 warps):
 //   warp 0      TMA producer: A tile 128x128 B, W tile 256x128 B (+ FP4 scale
 //               blocks) per 128-K stage into a 4-deep shared-memory ring;
 //   warp 1      allocates tensor memory and issues tcgen05.mma (one thread);
-//   warps 2..9  two epilogue warpgroups, each owning 128 of the 256 columns.
+//   warps 2, 3  idle;
+//   warps 4..11 two epilogue warpgroups, each owning 128 of the 256 columns.
+// The first warpgroup hands registers to the epilogue warpgroups with
+// setmaxnreg (launch: 384 x 168; after: 128 x 56 + 256 x 224 = 64512).
 // FP8 weights carry an fp32 scale per 128x128 block, which the block-scaled
 // MMA cannot apply (it takes power-of-two scale bytes), so each 128-K block
 // is multiplied without scaling into one of two TMEM partial buffers and the
@@ -39,12 +42,15 @@ namespace bsmoe {
 namespace {
 
 constexpr int kStages = 4;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
+constexpr int kEpiWarp0 = 4;  // warps 4..11 are the two epilogue warpgroups
 constexpr int kEpiThreads = 256;
 constexpr uint32_t kTileABytes = kBlockM * kBlockK;  // 16 KB
 constexpr uint32_t kTileBBytes = kBlockN * kBlockK;  // 32 KB (FP4 is unpacked to 1 B/elem in smem)
 constexpr uint32_t kSfaBytes = 512;
 constexpr uint32_t kSfbBytes = 1024;
+constexpr int kScaleSlots = 8;          // FP8: depth of the promotion-scale ring
+constexpr uint32_t kSwBytes = 32;       // FP8: 8 weight scales (one per 32 columns) per K block
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfTmemCol = 256;  // FP4: per stage 4 SFA + 8 SFB columns from here
 
@@ -58,9 +64,20 @@ struct __align__(1024) Smem {
   uint64_t tfull[2];
   uint64_t tempty[2];
   float amax_x[2][2][kBlockM];
+  // FP8 promotion scales, filled by the producer and released by the
+  // epilogue (its own ring: the MMA frees the operand stages before the
+  // epilogue reads the scales of that K block).
+  uint32_t sfa_w[kScaleSlots][kBlockM];
+  float sw[kScaleSlots][8];
+  uint64_t sfull[kScaleSlots];
+  uint64_t sempty[kScaleSlots];
   uint32_t tmem_base;
   int abort_flag;
 };
+
+static_assert(offsetof(Smem, sfa) % 16 == 0 && offsetof(Smem, sfb) % 16 == 0, "bulk copy alignment");
+static_assert(offsetof(Smem, sfa_w) % 16 == 0 && offsetof(Smem, sw) % 16 == 0, "bulk copy alignment");
+static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "shared memory budget");
 
 struct TileCoord {
   int e, mt, nt, row0, valid;
@@ -101,7 +118,19 @@ __device__ __forceinline__ bool epi_barrier_any(bool v) {
   return r != 0;
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+// silu(g) * u with the fast exponential and division (relative error a few
+// ulp of fp32; the result is requantized to e4m3 right after).
+__device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
+
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+
+// 2^(b - 127) for a UE8M0 byte b in [0, 254], built from the bits.
+__device__ __forceinline__ float ue8m0_to_float(uint32_t b) {
+  return b ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);
+}
 
 template <int FMT, bool GEMM1>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -126,6 +155,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
       mbar_init(&sm.tfull[b], 1);
       mbar_init(&sm.tempty[b], kEpiThreads / 32);
     }
+    for (int b = 0; b < kScaleSlots; ++b) {
+      mbar_init(&sm.sfull[b], 1);
+      mbar_init(&sm.sempty[b], kEpiThreads / 32);
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -137,7 +170,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
   tc_fence_after();
   const uint32_t tbase = sm.tmem_base;
 
-  if (warp == 0) {
+  if (warp < kEpiWarp0) {
+   regs_dec<56>();
+   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tmap_a);
@@ -148,10 +183,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
                                                 : kTileABytes + kTileBBytes;
       int stage = 0;
       uint32_t phase = 0;
+      int slot = 0;
+      uint32_t sphase = 0;
       for (int idx = blockIdx.x; idx < total_tiles && !*abort_flag; idx += gridDim.x) {
         const TileCoord c = decode_tile(idx, args.E, NT, mt_off, args.counts, args.padded_offsets);
         const int wrow = c.e * g.Np + c.nt * kBlockN;
         for (int kb = 0; kb < KB; ++kb) {
+          if constexpr (FMT == MOE_W_FP8) {
+            if (!mbar_wait(&sm.sempty[slot], sphase ^ 1, abort_flag)) break;
+            mbar_arrive_expect_tx(&sm.sfull[slot], kSfaBytes + kSwBytes);
+            bulk_load(sm.sfa_w[slot], args.a_sf + (static_cast<size_t>(c.row0 / kBlockM) * KB + kb) * kSfaBytes,
+                      kSfaBytes, &sm.sfull[slot]);
+            bulk_load(sm.sw[slot], args.w_scale + ((static_cast<size_t>(c.e) * NT + c.nt) * KB + kb) * kSwBytes,
+                      kSwBytes, &sm.sfull[slot]);
+            if (++slot == kScaleSlots) { slot = 0; sphase ^= 1; }
+          }
           if (!mbar_wait(&sm.empty[stage], phase ^ 1, abort_flag)) break;
           mbar_arrive_expect_tx(&sm.full[stage], bytes);
           tma_load_2d(sm.a[stage], &tmap_a, &sm.full[stage], kb * kBlockK, c.row0);
@@ -178,8 +224,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
         if constexpr (FMT == MOE_W_FP8) {
           constexpr uint32_t idesc = idesc_f8f6f4(0, 0, kBlockM, kBlockN);
           for (int kb = 0; kb < KB; ++kb) {
-            if (!mbar_wait(&sm.full[stage], phase, abort_flag)) break;
-            if (!mbar_wait(&sm.tempty[buf], bphase ^ 1, abort_flag)) break;
+            if (!mbar_wait_spin(&sm.full[stage], phase, abort_flag)) break;
+            if (!mbar_wait_spin(&sm.tempty[buf], bphase ^ 1, abort_flag)) break;
             tc_fence_after();
             const uint64_t ad = smem_desc(smem_u32(sm.a[stage]), 16, 1024, kSwizzle128B);
             const uint64_t bd = smem_desc(smem_u32(sm.b[stage]), 16, 1024, kSwizzle128B);
@@ -218,14 +264,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
         }
       }
     }
+   }
   } else {
+    regs_inc<224>();
     // ------------------------------------------------------------ epilogue
-    const int wg = (warp - 2) / 4;          // column half of the tile
+    const int wg = (warp - kEpiWarp0) / 4;  // column half of the tile
     const int quarter = warp & 3;           // TMEM lane quarter this warp may access
     const int m = quarter * 32 + lane;      // tile row owned by this thread
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     int buf = 0;
     uint32_t bphase = 0;
+    int sslot = 0;
+    uint32_t ssphase = 0;
     int tile_parity = 0;
     const float limit = args.swiglu_limit;
     const bool clamp = limit > 0.f && limit < INFINITY;
@@ -236,29 +286,40 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
       if constexpr (FMT == MOE_W_FP8) {
 #pragma unroll
         for (int i = 0; i < 128; ++i) acc[i] = 0.f;
-        const uint32_t* sfw = reinterpret_cast<const uint32_t*>(args.a_sf);
-        const float* wsc = reinterpret_cast<const float*>(args.w_scale) +
-                           (static_cast<size_t>(c.e) * (g.Np / 32) + (c.nt * kBlockN + wg * 128) / 32) * KB;
+        const int wi = 4 * (m % 32) + m / 32;  // this row's scale word in a 128-row block
         for (int kb = 0; kb < KB; ++kb) {
-          const uint32_t word = __ldg(sfw + sf_word_index(c.row0 + m, kb, KB));
-          float sw[4];
+          if (!mbar_wait(&sm.sfull[sslot], ssphase, abort_flag)) { ok = false; break; }
+          const float sa = ue8m0_to_float(sm.sfa_w[sslot][wi] & 0xFF);
+          float sc[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) sw[q] = __ldg(wsc + q * KB + kb);
-          const float sa = exp2f(static_cast<float>(static_cast<int>(word & 0xFF) - 127));
-          if (!mbar_wait(&sm.tfull[buf], bphase, abort_flag)) { ok = false; break; }
+          for (int q = 0; q < 4; ++q) sc[q] = sa * sm.sw[sslot][wg * 4 + q];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.sempty[sslot]);
+          if (++sslot == kScaleSlots) { sslot = 0; ssphase ^= 1; }
+          if (!mbar_wait_spin(&sm.tfull[buf], bphase, abort_flag)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(tbase + lane_base + buf * kBlockN + wg * 128 + q * 32, r);
+          for (int h = 0; h < 2; ++h) {
+            uint32_t r0[32], r1[32];
+            tmem_ld_32x32b_x32(tbase + lane_base + buf * kBlockN + wg * 128 + h * 64, r0);
+            tmem_ld_32x32b_x32(tbase + lane_base + buf * kBlockN + wg * 128 + h * 64 + 32, r1);
             tmem_wait_ld();
-            const float sc = sa * sw[q];
+            if (h == 1) {
+              // The partial is in registers: hand the buffer back to the MMA
+              // before the last FMAs.
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&sm.tempty[buf]);
+            }
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc[q * 32 + j] = fmaf(__uint_as_float(r[j]), sc, acc[q * 32 + j]);
+            for (int j = 0; j < 32; j += 2)
+              fma2_scalar(acc[h * 64 + j], acc[h * 64 + j + 1], __uint_as_float(r0[j]), __uint_as_float(r0[j + 1]),
+                          sc[2 * h]);
+#pragma unroll
+            for (int j = 0; j < 32; j += 2)
+              fma2_scalar(acc[h * 64 + 32 + j], acc[h * 64 + 33 + j], __uint_as_float(r1[j]),
+                          __uint_as_float(r1[j + 1]), sc[2 * h + 1]);
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.tempty[buf]);
           buf ^= 1;
           if (buf == 0) bphase ^= 1;
         }

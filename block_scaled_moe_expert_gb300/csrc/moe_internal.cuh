@@ -5,7 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "../../include/moe_experts.h"
+#include "moe_experts.h"
 
 namespace bsmoe {
 
@@ -33,7 +33,7 @@ struct GemmGeom {
 // Prepared weight layout (one of w13 / w2).
 struct PrepLayout {
   size_t codes_off, codes_bytes;  // u8 [E][Np][Kp] (FP8) or [E][Np][Kp/2] (FP4)
-  size_t scale_off, scale_bytes;  // FP8: f32 [E][Np/32][KB]; FP4: u32 chunks [E][NT][KB][256]
+  size_t scale_off, scale_bytes;  // FP8: f32 [E][NT][KB][8]; FP4: u32 chunks [E][NT][KB][256]
   size_t total;
 };
 

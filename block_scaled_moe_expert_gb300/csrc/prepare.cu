@@ -9,7 +9,9 @@
 //       tile rows [128,192) gate j = 128t + r - 64 [192,256) up j = 128t + r - 128
 //     (up j is original row I + j); rows with j >= I are zero;
 //   * K is padded to a multiple of 128 and N to a multiple of 256 with zeros;
-//   * FP8 block scales become one fp32 per (32 prepared rows, 128-K block);
+//   * FP8 block scales become one fp32 per (32 prepared rows, 128-K block),
+//     laid out [E][N tile][K block][8] so that the 8 scales of one tile and K
+//     block are 32 contiguous bytes;
 //   * FP4 UE8M0 scales become, per (expert, N tile, K block), the 1 KB image
 //     of the two 128-row scale blocks that tcgen05.cp copies into tensor
 //     memory: word(row r) at 4 * (r % 32) + r / 32, byte j = scale of the
@@ -86,17 +88,18 @@ __global__ void prep_codes_kernel(bool is_w13, const uint8_t* __restrict__ src, 
   }
 }
 
-// FP8 scales: out[e][g][kb] = scale[e][orig(32 g) / 128][kb] (0 for zero rows).
+// FP8 scales: out[e][nt][kb][j] = scale[e][orig(256 nt + 32 j) / 128][kb]
+// (0 for zero rows).
 __global__ void prep_scale_fp8_kernel(bool is_w13, const float* __restrict__ src, float* __restrict__ dst, int Np,
                                       int KB, int src_rb, int src_kb, int I, int H) {
   const int e = blockIdx.y;
-  const int n_groups = Np / 32;
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_groups * KB; i += gridDim.x * blockDim.x) {
-    const int g = i / KB, kb = i % KB;
-    const int o = orig_row(is_w13, g * 32, I, H);
+  const int NT = Np / 256;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < NT * KB * 8; i += gridDim.x * blockDim.x) {
+    const int j = i % 8, kb = (i / 8) % KB, nt = i / (8 * KB);
+    const int o = orig_row(is_w13, nt * 256 + j * 32, I, H);
     float v = 0.f;
     if (o >= 0 && kb < src_kb) v = src[(static_cast<size_t>(e) * src_rb + o / 128) * src_kb + kb];
-    dst[(static_cast<size_t>(e) * n_groups + g) * KB + kb] = v;
+    dst[static_cast<size_t>(e) * NT * KB * 8 + i] = v;
   }
 }
 
