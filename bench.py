@@ -58,6 +58,23 @@ def dist_env():
     return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def max_over_ranks(x, device="cpu"):
+    """Max of a float over all ranks (identity on one rank). Each rank is an
+    independent replica, so the job's time is the slowest rank's time."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_rank, world, seconds):
+    """Whole-job throughput: every rank processes the same per-rank work."""
+    return world * units_per_rank / seconds
+
+
 def weight_bytes_per_expert(wl, which):
     """Algorithmic bytes of one expert's weight (codes + scales)."""
     rows, k = (2 * wl.I, wl.H) if which == 13 else (wl.H, wl.I)
@@ -268,11 +285,7 @@ def run_ours(args, wl):
         barrier()
         t_wall1 = time.time()
     clocks = clk.summary(t_wall0, t_wall1)
-    total_ms = start.elapsed_time(stop)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(start.elapsed_time(stop), dev)
     ms_step = total_ms / args.steps
     stage_ms = {name: statistics.fmean(ev[i].elapsed_time(ev[i + 1]) for ev in stage_ev)
                 for i, name in enumerate(STAGES)}
@@ -298,8 +311,8 @@ def run_ours(args, wl):
             h_out.copy_(out, non_blocking=True)
         e1.record()
         torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / args.steps
-        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev) / args.steps
+        e2e = {"value": replica_throughput(flops, world, e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": hidden.numel() * 2 + idx.numel() * 4 + w.numel() * 4,
                "d2h_bytes_per_step": out.numel() * 2, "ms_per_step": e2e_ms}
 
@@ -325,7 +338,8 @@ def run_ours(args, wl):
         alg_units = "touched-expert weight bytes + activation bytes"
     roof.update({"kernel": dom, "traffic": None, "kernel_ms": stage_ms[dom], "algorithmic": alg_units})
 
-    line = {"metric": METRIC, "value": world * flops / (ms_step * 1e-3) / 1e12, "unit": UNIT, "n_gpus": world,
+    line = {"metric": METRIC, "value": replica_throughput(flops, world, ms_step * 1e-3) / 1e12, "unit": UNIT,
+            "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if wl.fmt == "fp8" else "e4m3xe2m1",
             "data": "synthetic",
@@ -333,7 +347,7 @@ def run_ours(args, wl):
                        "weights": wl.fmt, "swiglu_limit": wl.swiglu_limit, "pairs": pairs,
                        "touched_experts": touched, "parallelism": f"replicas{world}",
                        "l2": "inputs larger than L2 (expert weights stream from HBM every step)"},
-            "tokens_per_s": world * wl.T / (ms_step * 1e-3),
+            "tokens_per_s": replica_throughput(wl.T, world, ms_step * 1e-3),
             "stage_ms": stage_ms, "roofline": roof, "gpu_launches": 5 * args.steps, "clocks": clocks,
             "device_status": status}
     if e2e is not None:
