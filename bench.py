@@ -58,6 +58,29 @@ def dist_env():
     return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def measured_traffic(workload, kernel):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    GEMM kernel sources changed since the counters were taken."""
+    import glob
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic_full_size.json")) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    h = hashlib.sha256()
+    for src in d.get("sources", []):
+        try:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        except OSError:
+            return None
+    cur = sorted(glob.glob(os.path.join(ROOT, "block_scaled_moe_expert_gb300", "csrc", "*.cuh")))
+    if len(cur) + 1 != len(d.get("sources", [])) or h.hexdigest() != d.get("kernel_source_sha256"):
+        return None
+    return d.get("bytes_per_launch", {}).get(workload, {}).get(kernel)
+
+
 def max_over_ranks(x, device="cpu"):
     """Max of a float over all ranks (identity on one rank). Each rank is an
     independent replica, so the job's time is the slowest rank's time."""
@@ -336,7 +359,9 @@ def run_ours(args, wl):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_source": f"{peak_src}: copy bandwidth"}
         alg_units = "touched-expert weight bytes + activation bytes"
-    roof.update({"kernel": dom, "traffic": None, "kernel_ms": stage_ms[dom], "algorithmic": alg_units})
+    traffic = measured_traffic(wl.name, dom)
+    roof.update({"kernel": dom, "traffic": traffic, "traffic_unit": "bytes per launch" if traffic else None,
+                 "kernel_ms": stage_ms[dom], "algorithmic": alg_units})
 
     line = {"metric": METRIC, "value": replica_throughput(flops, world, ms_step * 1e-3) / 1e12, "unit": UNIT,
             "n_gpus": world,
