@@ -49,7 +49,8 @@ constexpr uint32_t kTileABytes = kBlockM * kBlockK;  // 16 KB
 constexpr uint32_t kTileBBytes = kBlockN * kBlockK;  // 32 KB (FP4 is unpacked to 1 B/elem in smem)
 constexpr uint32_t kSfaBytes = 512;
 constexpr uint32_t kSfbBytes = 1024;
-constexpr int kScaleSlots = 8;          // FP8: depth of the promotion-scale ring
+constexpr int kScaleSlots = 4;          // FP8: slots of the promotion-scale ring
+constexpr int kScaleGroup = 4;          // FP8: K blocks per slot
 constexpr uint32_t kSwBytes = 32;       // FP8: 8 weight scales (one per 32 columns) per K block
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfTmemCol = 256;  // FP4: per stage 4 SFA + 8 SFB columns from here
@@ -67,8 +68,8 @@ struct __align__(1024) Smem {
   // FP8 promotion scales, filled by the producer and released by the
   // epilogue (its own ring: the MMA frees the operand stages before the
   // epilogue reads the scales of that K block).
-  uint32_t sfa_w[kScaleSlots][kBlockM];
-  float sw[kScaleSlots][8];
+  uint32_t sfa_w[kScaleSlots][kScaleGroup][kBlockM];
+  float sw[kScaleSlots][kScaleGroup][8];
   uint64_t sfull[kScaleSlots];
   uint64_t sempty[kScaleSlots];
   uint32_t tmem_base;
@@ -183,21 +184,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
                                                 : kTileABytes + kTileBBytes;
       int stage = 0;
       uint32_t phase = 0;
-      int slot = 0;
-      uint32_t sphase = 0;
       for (int idx = blockIdx.x; idx < total_tiles && !*abort_flag; idx += gridDim.x) {
         const TileCoord c = decode_tile(idx, args.E, NT, mt_off, args.counts, args.padded_offsets);
         const int wrow = c.e * g.Np + c.nt * kBlockN;
         for (int kb = 0; kb < KB; ++kb) {
-          if constexpr (FMT == MOE_W_FP8) {
-            if (!mbar_wait(&sm.sempty[slot], sphase ^ 1, abort_flag)) break;
-            mbar_arrive_expect_tx(&sm.sfull[slot], kSfaBytes + kSwBytes);
-            bulk_load(sm.sfa_w[slot], args.a_sf + (static_cast<size_t>(c.row0 / kBlockM) * KB + kb) * kSfaBytes,
-                      kSfaBytes, &sm.sfull[slot]);
-            bulk_load(sm.sw[slot], args.w_scale + ((static_cast<size_t>(c.e) * NT + c.nt) * KB + kb) * kSwBytes,
-                      kSwBytes, &sm.sfull[slot]);
-            if (++slot == kScaleSlots) { slot = 0; sphase ^= 1; }
-          }
           if (!mbar_wait(&sm.empty[stage], phase ^ 1, abort_flag)) break;
           mbar_arrive_expect_tx(&sm.full[stage], bytes);
           tma_load_2d(sm.a[stage], &tmap_a, &sm.full[stage], kb * kBlockK, c.row0);
@@ -264,6 +254,28 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
         }
       }
     }
+   } else if (warp == 2 && FMT == MOE_W_FP8) {
+    // ------------------------------------------------------ scale producer
+    // Promotion scales for kScaleGroup consecutive K blocks per slot: the
+    // activation exponent words of the 128 rows and the 8 weight scales.
+    // Both are contiguous in K for a tile, so a slot is two bulk copies.
+    if (lane == 0) {
+      int slot = 0;
+      uint32_t sphase = 0;
+      for (int idx = blockIdx.x; idx < total_tiles && !*abort_flag; idx += gridDim.x) {
+        const TileCoord c = decode_tile(idx, args.E, NT, mt_off, args.counts, args.padded_offsets);
+        for (int kb0 = 0; kb0 < KB; kb0 += kScaleGroup) {
+          const int n = min(kScaleGroup, KB - kb0);
+          if (!mbar_wait(&sm.sempty[slot], sphase ^ 1, abort_flag)) break;
+          mbar_arrive_expect_tx(&sm.sfull[slot], n * (kSfaBytes + kSwBytes));
+          bulk_load(sm.sfa_w[slot], args.a_sf + (static_cast<size_t>(c.row0 / kBlockM) * KB + kb0) * kSfaBytes,
+                    n * kSfaBytes, &sm.sfull[slot]);
+          bulk_load(sm.sw[slot], args.w_scale + ((static_cast<size_t>(c.e) * NT + c.nt) * KB + kb0) * kSwBytes,
+                    n * kSwBytes, &sm.sfull[slot]);
+          if (++slot == kScaleSlots) { slot = 0; sphase ^= 1; }
+        }
+      }
+    }
    }
   } else {
     regs_inc<224>();
@@ -288,14 +300,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
         for (int i = 0; i < 128; ++i) acc[i] = 0.f;
         const int wi = 4 * (m % 32) + m / 32;  // this row's scale word in a 128-row block
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(&sm.sfull[sslot], ssphase, abort_flag)) { ok = false; break; }
-          const float sa = ue8m0_to_float(sm.sfa_w[sslot][wi] & 0xFF);
+          const int gi = kb % kScaleGroup;
+          if (gi == 0 && !mbar_wait_spin(&sm.sfull[sslot], ssphase, abort_flag)) { ok = false; break; }
+          const float sa = ue8m0_to_float(sm.sfa_w[sslot][gi][wi] & 0xFF);
           float sc[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) sc[q] = sa * sm.sw[sslot][wg * 4 + q];
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.sempty[sslot]);
-          if (++sslot == kScaleSlots) { sslot = 0; ssphase ^= 1; }
+          for (int q = 0; q < 4; ++q) sc[q] = sa * sm.sw[sslot][gi][wg * 4 + q];
+          if (gi == kScaleGroup - 1 || kb == KB - 1) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.sempty[sslot]);
+            if (++sslot == kScaleSlots) { sslot = 0; ssphase ^= 1; }
+          }
           if (!mbar_wait_spin(&sm.tfull[buf], bphase, abort_flag)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
