@@ -385,13 +385,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
         if (m < c.valid) {
           uint8_t* dst = args.out_q + static_cast<size_t>(row) * args.out_cols + c.nt * 128 + wg * 64;
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 pk;
-            pk.x = pack4_e4m3(acc[16 * v + 0] * s, acc[16 * v + 1] * s, acc[16 * v + 2] * s, acc[16 * v + 3] * s);
-            pk.y = pack4_e4m3(acc[16 * v + 4] * s, acc[16 * v + 5] * s, acc[16 * v + 6] * s, acc[16 * v + 7] * s);
-            pk.z = pack4_e4m3(acc[16 * v + 8] * s, acc[16 * v + 9] * s, acc[16 * v + 10] * s, acc[16 * v + 11] * s);
-            pk.w = pack4_e4m3(acc[16 * v + 12] * s, acc[16 * v + 13] * s, acc[16 * v + 14] * s, acc[16 * v + 15] * s);
-            *reinterpret_cast<uint4*>(dst + 16 * v) = pk;
+          for (int v = 0; v < 2; ++v) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const float* a4 = acc + 32 * v + 4 * u;
+              pk[u] = pack4_e4m3(a4[0] * s, a4[1] * s, a4[2] * s, a4[3] * s);
+            }
+            st_global_v8(dst + 32 * v, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
           }
           if (wg == 0)
             reinterpret_cast<uint32_t*>(args.out_sf)[sf_word_index(row, c.nt, args.out_blocks)] =
@@ -405,11 +406,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
           const int col0 = c.nt * kBlockN + wg * 128;
           float* dst = args.out_y + static_cast<size_t>(row) * args.H + col0;
 #pragma unroll
-          for (int v = 0; v < 32; ++v) {
-            if (col0 + 4 * v < args.H) {
-              float4 o = make_float4(acc[4 * v] * wgt, acc[4 * v + 1] * wgt, acc[4 * v + 2] * wgt,
-                                     acc[4 * v + 3] * wgt);
-              *reinterpret_cast<float4*>(dst + 4 * v) = o;
+          for (int v = 0; v < 16; ++v) {
+            if (col0 + 8 * v < args.H) {
+              const float* a8 = acc + 8 * v;
+              st_global_v8(dst + 8 * v, __float_as_uint(a8[0] * wgt), __float_as_uint(a8[1] * wgt),
+                           __float_as_uint(a8[2] * wgt), __float_as_uint(a8[3] * wgt), __float_as_uint(a8[4] * wgt),
+                           __float_as_uint(a8[5] * wgt), __float_as_uint(a8[6] * wgt), __float_as_uint(a8[7] * wgt));
             }
           }
         }

@@ -102,6 +102,15 @@ __device__ __forceinline__ void fma2_scalar(float& d0, float& d1, float a0, floa
       : "f"(a0), "f"(a1), "f"(s));
 }
 
+// 32-byte store of eight 32-bit values (address 32-byte aligned): one full
+// L2 sector per thread and half the store instructions of 16-byte stores.
+__device__ __forceinline__ void st_global_v8(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t e,
+                                             uint32_t f, uint32_t g, uint32_t h) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d),
+               "r"(e), "r"(f), "r"(g), "r"(h)
+               : "memory");
+}
+
 // ------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
