@@ -130,6 +130,7 @@ bool ws_layout(int fmt, int T, int H, int I, int E, int K, WsLayout* out) {
   p.act = take(static_cast<size_t>(M) * g2.Kp);
   p.asf = take(4ull * M * g2.KB);
   p.y = take(4ull * M * H);
+  L.route_scratch = take(4ull * (static_cast<size_t>(route_chunks(static_cast<int>(S))) + 1) * (E + 1));
   p.total_bytes = off;
   p.row_capacity = static_cast<int32_t>(M);
   p.row_align = kRowAlign;

@@ -44,7 +44,11 @@ GemmGeom geom_w2(int H, int I);
 struct WsLayout {
   moe_workspace_layout pub;
   int S, M, max_m_tiles;
+  size_t route_scratch;  // int32 [chunks][E + 1] for the multi-CTA routing
 };
+
+// Number of routing chunks for S slots (0: the single-CTA kernel is used).
+int route_chunks(int S);
 bool ws_layout(int fmt, int T, int H, int I, int E, int K, WsLayout* out);
 
 // Offsets inside the int32 "tiles" region.

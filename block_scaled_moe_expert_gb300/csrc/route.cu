@@ -21,11 +21,12 @@ namespace {
 
 constexpr int kWarps = 32;
 constexpr int kThreads = kWarps * 32;
+constexpr int kSingleCtaSlots = 4096;  // up to this many slots one CTA routes everything
 
 __device__ __forceinline__ int slot_key(const int32_t* idx, int s, int E, uint32_t* status) {
   int v = __ldg(idx + s);
   if (v >= 0 && v < E) return v;
-  if (v != -1) atomicOr(status, MOE_DEV_BAD_EXPERT_ID);
+  if (v != -1 && status != nullptr) atomicOr(status, MOE_DEV_BAD_EXPERT_ID);
   return E;
 }
 
@@ -158,10 +159,168 @@ route_kernel(const int32_t* __restrict__ idx, int S, int E, int M, int32_t* __re
   (void)M;
 }
 
+// ---------------------------------------------------------------------------
+// Multi-CTA path for large S: the slots are split into chunks of
+// kChunk consecutive slots. (1) every chunk counts its keys; (2) one CTA
+// turns the per-chunk counts into, for each key, the number of equal keys in
+// earlier chunks, and computes the per-expert totals and offsets; (3) every
+// chunk places its slots with the same per-warp stable ranking as above.
+// The placement is identical to the single-CTA kernel's.
+
+constexpr int kChunk = 2048;
+constexpr int kChunkWarps = 8;
+
+__global__ void __launch_bounds__(kChunkWarps * 32)
+route_hist_kernel(const int32_t* __restrict__ idx, int S, int E, int32_t* __restrict__ chunk_hist,
+                  uint32_t* __restrict__ status) {
+  extern __shared__ int h[];  // [E + 1]
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) h[i] = 0;
+  __syncthreads();
+  const int beg = blockIdx.x * kChunk, end = min(S, beg + kChunk);
+  for (int s = beg + threadIdx.x; s < end; s += blockDim.x) atomicAdd(&h[slot_key(idx, s, E, status)], 1);
+  __syncthreads();
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) chunk_hist[static_cast<size_t>(blockIdx.x) * (E + 1) + i] = h[i];
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+route_scan_kernel(int E, int G, int32_t* __restrict__ chunk_hist, int32_t* __restrict__ counts,
+                  int32_t* __restrict__ offsets, int32_t* __restrict__ padded_offsets,
+                  int32_t* __restrict__ row_slot, int32_t* __restrict__ tiles) {
+  __shared__ int warp_sums[32];
+  __shared__ int tot[3];
+  __shared__ int s_off[kMaxExperts + 1];
+  __shared__ int s_pad[kMaxExperts + 1];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int cnt = 0;
+  if (tid <= E) {  // exclusive prefix over chunks, in place
+    int run = 0;
+    for (int g = 0; g < G; ++g) {
+      int32_t* c = chunk_hist + static_cast<size_t>(g) * (E + 1) + tid;
+      const int v = *c;
+      *c = run;
+      run += v;
+    }
+    cnt = run;
+  }
+  const int c_e = (tid < E) ? cnt : 0;
+  const int off = block_excl_scan(c_e, warp_sums, &tot[0]);
+  const int pad = block_excl_scan((c_e + kRowAlign - 1) / kRowAlign * kRowAlign, warp_sums, &tot[1]);
+  const int mts = block_excl_scan((c_e + kBlockM - 1) / kBlockM, warp_sums, &tot[2]);
+  if (tid < E) {
+    counts[tid] = c_e;
+    offsets[tid] = off;
+    padded_offsets[tid] = pad;
+    tiles[kTilesHdr + tid] = mts;
+    s_off[tid] = off;
+    s_pad[tid] = pad;
+  }
+  if (tid == 0) {
+    offsets[E] = tot[0];
+    padded_offsets[E] = tot[1];
+    tiles[kTilesHdr + E] = tot[2];
+    tiles[0] = tot[2];
+    s_off[E] = tot[0];
+    s_pad[E] = tot[1];
+  }
+  __syncthreads();
+  for (int e = warp; e < E; e += kWarps) {
+    const int lo = s_pad[e] + (s_off[e + 1] - s_off[e]);
+    const int hi = s_pad[e + 1];
+    for (int r = lo + lane; r < hi; r += 32) row_slot[r] = -1;
+  }
+}
+
+__global__ void __launch_bounds__(kChunkWarps * 32)
+route_scatter_kernel(const int32_t* __restrict__ idx, int S, int E, const int32_t* __restrict__ chunk_base,
+                     const int32_t* __restrict__ offsets, const int32_t* __restrict__ padded_offsets,
+                     int32_t* __restrict__ perm, int32_t* __restrict__ inv, int32_t* __restrict__ row_slot) {
+  extern __shared__ int smem[];
+  const int stride = E + 1;
+  int* hist = smem;                       // [kChunkWarps][E + 1]
+  int* s_off = smem + kChunkWarps * stride;  // [E + 1]
+  int* s_pad = s_off + stride;               // [E + 1]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < kChunkWarps * stride; i += blockDim.x) hist[i] = 0;
+  for (int i = tid; i <= E; i += blockDim.x) {
+    s_off[i] = offsets[i];
+    s_pad[i] = padded_offsets[i];
+  }
+  __syncthreads();
+  const int cbeg = blockIdx.x * kChunk, cend = min(S, cbeg + kChunk);
+  const int per = kChunk / kChunkWarps;
+  const int beg = cbeg + warp * per, end = min(cend, beg + per);
+  int* h = hist + warp * stride;
+  for (int base = beg; base < end; base += 32) {
+    const int s = base + lane;
+    const unsigned active = __ballot_sync(0xffffffffu, s < end);
+    if (s < end) {
+      const int key = slot_key(idx, s, E, nullptr);
+      const unsigned peers = __match_any_sync(active, key);
+      if (lane == __ffs(peers) - 1) h[key] += __popc(peers);
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  // per key: chunk base (equal keys in earlier chunks) + equal keys in earlier warps
+  const int32_t* cb = chunk_base + static_cast<size_t>(blockIdx.x) * stride;
+  for (int k = tid; k <= E; k += blockDim.x) {
+    int run = cb[k];
+    for (int w = 0; w < kChunkWarps; ++w) {
+      const int c = hist[w * stride + k];
+      hist[w * stride + k] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  for (int base = beg; base < end; base += 32) {
+    const int s = base + lane;
+    const unsigned active = __ballot_sync(0xffffffffu, s < end);
+    if (s < end) {
+      const int key = slot_key(idx, s, E, nullptr);
+      const unsigned peers = __match_any_sync(active, key);
+      const int leader = __ffs(peers) - 1;
+      const int pos = h[key] + __popc(peers & ((1u << lane) - 1u));
+      __syncwarp(active);
+      if (lane == leader) h[key] += __popc(peers);
+      perm[s_off[key] + pos] = s;
+      if (key < E) {
+        const int row = s_pad[key] + pos;
+        inv[s] = row;
+        row_slot[row] = s;
+      } else {
+        inv[s] = -1;
+      }
+    }
+    __syncwarp();
+  }
+}
+
+__global__ void clear_status_kernel(uint32_t* status) { *status = 0u; }
+
 }  // namespace
+
+int route_chunks(int S) { return S <= kSingleCtaSlots ? 0 : (S + kChunk - 1) / kChunk; }
 
 cudaError_t launch_route(const int32_t* topk_idx, int S, int E, const WsLayout& L, uint8_t* ws, cudaStream_t st) {
   const moe_workspace_layout& p = L.pub;
+  const int G = route_chunks(S);
+  if (G > 0) {
+    int32_t* chunk_hist = reinterpret_cast<int32_t*>(ws + L.route_scratch);
+    uint32_t* status = reinterpret_cast<uint32_t*>(ws + p.status);
+    clear_status_kernel<<<1, 1, 0, st>>>(status);
+    route_hist_kernel<<<G, kChunkWarps * 32, sizeof(int) * (E + 1), st>>>(topk_idx, S, E, chunk_hist, status);
+    route_scan_kernel<<<1, kThreads, 0, st>>>(E, G, chunk_hist, reinterpret_cast<int32_t*>(ws + p.counts),
+                                              reinterpret_cast<int32_t*>(ws + p.offsets),
+                                              reinterpret_cast<int32_t*>(ws + p.padded_offsets),
+                                              reinterpret_cast<int32_t*>(ws + p.row_slot),
+                                              reinterpret_cast<int32_t*>(ws + p.tiles));
+    const size_t smem = sizeof(int) * (kChunkWarps + 2) * (E + 1);
+    route_scatter_kernel<<<G, kChunkWarps * 32, smem, st>>>(
+        topk_idx, S, E, chunk_hist, reinterpret_cast<const int32_t*>(ws + p.offsets),
+        reinterpret_cast<const int32_t*>(ws + p.padded_offsets), reinterpret_cast<int32_t*>(ws + p.perm),
+        reinterpret_cast<int32_t*>(ws + p.inv), reinterpret_cast<int32_t*>(ws + p.row_slot));
+    return cudaGetLastError();
+  }
   const size_t smem = sizeof(int) * kWarps * (E + 1);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
