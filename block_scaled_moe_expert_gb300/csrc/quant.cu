@@ -24,7 +24,10 @@ namespace {
 
 constexpr int kQuantWarps = 8;
 
-// One CTA per token; warp w handles 128-column blocks w, w + 8, ...
+// One CTA per token. A warp covers 256 columns (two 128-column blocks) per
+// step: each lane loads 8 bf16 (16 bytes), the 16 lanes of a half-warp reduce
+// the block's amax, and each lane stores 8 code bytes per destination row, so
+// a warp writes 256 contiguous bytes of every row it copies to.
 __global__ void __launch_bounds__(kQuantWarps * 32)
 quant_permute_kernel(const __nv_bfloat16* __restrict__ hidden, int H, int K, int Kp,
                      const int32_t* __restrict__ inv, uint8_t* __restrict__ xq, uint32_t* __restrict__ xsf) {
@@ -45,29 +48,36 @@ quant_permute_kernel(const __nv_bfloat16* __restrict__ hidden, int H, int K, int
   const int n = nrows;
   if (n == 0) return;
   const __nv_bfloat16* xr = hidden + static_cast<size_t>(t) * H;
-  for (int b = warp; b < nblk; b += kQuantWarps) {
-    const int c0 = b * 128 + lane * 4;
-    float v[4] = {0.f, 0.f, 0.f, 0.f};
-    if (c0 < H) {  // H % 64 == 0, so a lane's 4 columns are all in or all out
-      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(xr + c0));
-      const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-      const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-      v[0] = __low2float(p0);
-      v[1] = __high2float(p0);
-      v[2] = __low2float(p1);
-      v[3] = __high2float(p1);
-    }
-    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+  for (int c0w = warp * 256; c0w < Kp; c0w += kQuantWarps * 256) {
+    const int c0 = c0w + lane * 8;
+    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (c0 < H) {  // H % 64 == 0: a lane's 8 columns are all in or all out
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(xr + c0));
+      const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __low2float(p2[i]);
+        v[2 * i + 1] = __high2float(p2[i]);
+      }
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const int e = act_exponent(amax);
     const float s = exp2_neg(e);
-    const uint32_t q = pack4_e4m3(v[0] * s, v[1] * s, v[2] * s, v[3] * s);
+    const uint2 q = make_uint2(pack4_e4m3(v[0] * s, v[1] * s, v[2] * s, v[3] * s),
+                               pack4_e4m3(v[4] * s, v[5] * s, v[6] * s, v[7] * s));
     const uint32_t word = static_cast<uint32_t>(e + 127) * 0x01010101u;
+    const bool in_range = c0 < Kp;
+    const int blk = c0 / 128;
     for (int i = 0; i < n; ++i) {
       const int r = rows[i];
-      *reinterpret_cast<uint32_t*>(xq + static_cast<size_t>(r) * Kp + c0) = q;
-      if (lane == 0) xsf[sf_word_index(r, b, nblk)] = word;
+      if (in_range) {
+        *reinterpret_cast<uint2*>(xq + static_cast<size_t>(r) * Kp + c0) = q;
+        if ((lane & 15) == 0) xsf[sf_word_index(r, blk, nblk)] = word;
+      }
     }
   }
 }

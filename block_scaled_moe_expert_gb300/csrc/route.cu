@@ -8,7 +8,7 @@
 // an id outside [-1, E), which also raises MOE_DEV_BAD_EXPERT_ID) takes key E
 // so it sorts after every group.
 //
-// One CTA of 32 warps. Warp w owns a contiguous range of slots and walks it
+// Up to 8192 slots: one CTA of 32 warps. Warp w owns a contiguous range of slots and walks it
 // 32 slots at a time; __match_any_sync groups equal keys inside a step, so a
 // slot's rank is (#equal keys in earlier warps) + (#equal keys earlier in its
 // own warp), which is exactly the stable order. No data atomics are used:
@@ -21,7 +21,7 @@ namespace {
 
 constexpr int kWarps = 32;
 constexpr int kThreads = kWarps * 32;
-constexpr int kSingleCtaSlots = 4096;  // up to this many slots one CTA routes everything
+constexpr int kSingleCtaSlots = 8192;  // up to this many slots one CTA routes everything
 
 __device__ __forceinline__ int slot_key(const int32_t* idx, int s, int E, uint32_t* status) {
   int v = __ldg(idx + s);
@@ -171,13 +171,12 @@ constexpr int kChunk = 2048;
 constexpr int kChunkWarps = 8;
 
 __global__ void __launch_bounds__(kChunkWarps * 32)
-route_hist_kernel(const int32_t* __restrict__ idx, int S, int E, int32_t* __restrict__ chunk_hist,
-                  uint32_t* __restrict__ status) {
+route_hist_kernel(const int32_t* __restrict__ idx, int S, int E, int32_t* __restrict__ chunk_hist) {
   extern __shared__ int h[];  // [E + 1]
   for (int i = threadIdx.x; i <= E; i += blockDim.x) h[i] = 0;
   __syncthreads();
   const int beg = blockIdx.x * kChunk, end = min(S, beg + kChunk);
-  for (int s = beg + threadIdx.x; s < end; s += blockDim.x) atomicAdd(&h[slot_key(idx, s, E, status)], 1);
+  for (int s = beg + threadIdx.x; s < end; s += blockDim.x) atomicAdd(&h[slot_key(idx, s, E, nullptr)], 1);
   __syncthreads();
   for (int i = threadIdx.x; i <= E; i += blockDim.x) chunk_hist[static_cast<size_t>(blockIdx.x) * (E + 1) + i] = h[i];
 }
@@ -185,12 +184,15 @@ route_hist_kernel(const int32_t* __restrict__ idx, int S, int E, int32_t* __rest
 __global__ void __launch_bounds__(kThreads, 1)
 route_scan_kernel(int E, int G, int32_t* __restrict__ chunk_hist, int32_t* __restrict__ counts,
                   int32_t* __restrict__ offsets, int32_t* __restrict__ padded_offsets,
-                  int32_t* __restrict__ row_slot, int32_t* __restrict__ tiles) {
+                  int32_t* __restrict__ row_slot, int32_t* __restrict__ tiles, uint32_t* __restrict__ status) {
   __shared__ int warp_sums[32];
   __shared__ int tot[3];
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_pad[kMaxExperts + 1];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // The status word reflects the most recent forward; the scatter kernel
+  // raises the invalid-id flag after this.
+  if (tid == 0) *status = 0u;
   int cnt = 0;
   if (tid <= E) {  // exclusive prefix over chunks, in place
     int run = 0;
@@ -233,7 +235,8 @@ route_scan_kernel(int E, int G, int32_t* __restrict__ chunk_hist, int32_t* __res
 __global__ void __launch_bounds__(kChunkWarps * 32)
 route_scatter_kernel(const int32_t* __restrict__ idx, int S, int E, const int32_t* __restrict__ chunk_base,
                      const int32_t* __restrict__ offsets, const int32_t* __restrict__ padded_offsets,
-                     int32_t* __restrict__ perm, int32_t* __restrict__ inv, int32_t* __restrict__ row_slot) {
+                     int32_t* __restrict__ perm, int32_t* __restrict__ inv, int32_t* __restrict__ row_slot,
+                     uint32_t* __restrict__ status) {
   extern __shared__ int smem[];
   const int stride = E + 1;
   int* hist = smem;                       // [kChunkWarps][E + 1]
@@ -254,7 +257,7 @@ route_scatter_kernel(const int32_t* __restrict__ idx, int S, int E, const int32_
     const int s = base + lane;
     const unsigned active = __ballot_sync(0xffffffffu, s < end);
     if (s < end) {
-      const int key = slot_key(idx, s, E, nullptr);
+      const int key = slot_key(idx, s, E, status);
       const unsigned peers = __match_any_sync(active, key);
       if (lane == __ffs(peers) - 1) h[key] += __popc(peers);
     }
@@ -295,8 +298,6 @@ route_scatter_kernel(const int32_t* __restrict__ idx, int S, int E, const int32_
   }
 }
 
-__global__ void clear_status_kernel(uint32_t* status) { *status = 0u; }
-
 }  // namespace
 
 int route_chunks(int S) { return S <= kSingleCtaSlots ? 0 : (S + kChunk - 1) / kChunk; }
@@ -307,18 +308,17 @@ cudaError_t launch_route(const int32_t* topk_idx, int S, int E, const WsLayout& 
   if (G > 0) {
     int32_t* chunk_hist = reinterpret_cast<int32_t*>(ws + L.route_scratch);
     uint32_t* status = reinterpret_cast<uint32_t*>(ws + p.status);
-    clear_status_kernel<<<1, 1, 0, st>>>(status);
-    route_hist_kernel<<<G, kChunkWarps * 32, sizeof(int) * (E + 1), st>>>(topk_idx, S, E, chunk_hist, status);
+    route_hist_kernel<<<G, kChunkWarps * 32, sizeof(int) * (E + 1), st>>>(topk_idx, S, E, chunk_hist);
     route_scan_kernel<<<1, kThreads, 0, st>>>(E, G, chunk_hist, reinterpret_cast<int32_t*>(ws + p.counts),
                                               reinterpret_cast<int32_t*>(ws + p.offsets),
                                               reinterpret_cast<int32_t*>(ws + p.padded_offsets),
                                               reinterpret_cast<int32_t*>(ws + p.row_slot),
-                                              reinterpret_cast<int32_t*>(ws + p.tiles));
+                                              reinterpret_cast<int32_t*>(ws + p.tiles), status);
     const size_t smem = sizeof(int) * (kChunkWarps + 2) * (E + 1);
     route_scatter_kernel<<<G, kChunkWarps * 32, smem, st>>>(
         topk_idx, S, E, chunk_hist, reinterpret_cast<const int32_t*>(ws + p.offsets),
         reinterpret_cast<const int32_t*>(ws + p.padded_offsets), reinterpret_cast<int32_t*>(ws + p.perm),
-        reinterpret_cast<int32_t*>(ws + p.inv), reinterpret_cast<int32_t*>(ws + p.row_slot));
+        reinterpret_cast<int32_t*>(ws + p.inv), reinterpret_cast<int32_t*>(ws + p.row_slot), status);
     return cudaGetLastError();
   }
   const size_t smem = sizeof(int) * kWarps * (E + 1);

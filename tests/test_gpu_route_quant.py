@@ -48,8 +48,8 @@ CASES = [
     P.W.scaled(P.W.WORKLOADS["dsv3_decode_fp8"], T=512, H=256, I=128),
     P.W.scaled(P.W.WORKLOADS["gptoss_fp8xfp4"], T=333, H=2880, I=128, E=16),
     P.W.scaled(P.W.WORKLOADS["dsv3_decode_fp4_T1"], H=512, I=256),
-    # more than 4096 slots: the multi-CTA routing path (4 and 17 chunks)
-    P.W.scaled(P.W.WORKLOADS["dsv3_decode_fp8"], T=1000, H=256, I=128),
+    # more than 8192 slots: the multi-CTA routing path (5 and 17 chunks)
+    P.W.scaled(P.W.WORKLOADS["dsv3_decode_fp8"], T=1250, H=256, I=128),
     P.W.scaled(P.W.WORKLOADS["gptoss_fp8xfp4"], T=8500, H=256, I=128, E=128),
 ]
 
@@ -61,7 +61,7 @@ def test_route_and_quant_bit_exact(wl):
     assert P.B.device_status(r["ws"]) == 0
 
 
-@pytest.mark.parametrize("T", [40, 3000])
+@pytest.mark.parametrize("T", [40, 5000])
 def test_invalid_ids_are_skipped_and_flagged(T):
     wl = P.W.scaled(P.W.WORKLOADS["tiny_fp8"], T=T)
     idx, w = P.W.make_routing(wl, "cuda")
