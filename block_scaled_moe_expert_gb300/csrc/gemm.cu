@@ -133,6 +133,10 @@ __device__ __forceinline__ float ue8m0_to_float(uint32_t b) {
   return b ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);
 }
 
+// Element i of the thread's 128 accumulators, held as 64 fp32 pairs so the
+// promotion can use packed fp32x2 FMAs without re-pairing registers.
+#define ACC(i) (((i) & 1) ? acc2[(i) >> 1].y : acc2[(i) >> 1].x)
+
 template <int FMT, bool GEMM1>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
@@ -293,19 +297,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
     const bool clamp = limit > 0.f && limit < INFINITY;
     for (int idx = blockIdx.x; idx < total_tiles && !*abort_flag; idx += gridDim.x) {
       const TileCoord c = decode_tile(idx, args.E, NT, mt_off, args.counts, args.padded_offsets);
-      float acc[128];
+      float2 acc2[64];
       bool ok = true;
       if constexpr (FMT == MOE_W_FP8) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i) acc[i] = 0.f;
+        for (int i = 0; i < 64; ++i) acc2[i] = make_float2(0.f, 0.f);
         const int wi = 4 * (m % 32) + m / 32;  // this row's scale word in a 128-row block
         for (int kb = 0; kb < KB; ++kb) {
           const int gi = kb % kScaleGroup;
           if (gi == 0 && !mbar_wait_spin(&sm.sfull[sslot], ssphase, abort_flag)) { ok = false; break; }
           const float sa = ue8m0_to_float(sm.sfa_w[sslot][gi][wi] & 0xFF);
-          float sc[4];
+          float2 sc2[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) sc[q] = sa * sm.sw[sslot][gi][wg * 4 + q];
+          for (int q = 0; q < 4; ++q) {
+            const float v = sa * sm.sw[sslot][gi][wg * 4 + q];
+            sc2[q] = make_float2(v, v);
+          }
           if (gi == kScaleGroup - 1 || kb == KB - 1) {
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.sempty[sslot]);
@@ -327,13 +334,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
               if (lane == 0) mbar_arrive(&sm.tempty[buf]);
             }
 #pragma unroll
-            for (int j = 0; j < 32; j += 2)
-              fma2_scalar(acc[h * 64 + j], acc[h * 64 + j + 1], __uint_as_float(r0[j]), __uint_as_float(r0[j + 1]),
-                          sc[2 * h]);
+            for (int j = 0; j < 16; ++j)
+              acc2[h * 32 + j] = __ffma2_rn(make_float2(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1])),
+                                            sc2[2 * h], acc2[h * 32 + j]);
 #pragma unroll
-            for (int j = 0; j < 32; j += 2)
-              fma2_scalar(acc[h * 64 + 32 + j], acc[h * 64 + 33 + j], __uint_as_float(r1[j]),
-                          __uint_as_float(r1[j + 1]), sc[2 * h + 1]);
+            for (int j = 0; j < 16; ++j)
+              acc2[h * 32 + 16 + j] =
+                  __ffma2_rn(make_float2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1])), sc2[2 * h + 1],
+                             acc2[h * 32 + 16 + j]);
           }
           buf ^= 1;
           if (buf == 0) bphase ^= 1;
@@ -348,7 +356,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
             tmem_ld_32x32b_x32(tbase + lane_base + wg * 128 + q * 32, r);
             tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc[q * 32 + j] = __uint_as_float(r[j]);
+            for (int j = 0; j < 16; ++j)
+              acc2[q * 16 + j] = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
           }
           tc_fence_before();
           __syncwarp();
@@ -358,19 +367,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
       }
       const int row = c.row0 + m;
       if constexpr (GEMM1) {
-        // acc[0..63] = gate, acc[64..127] = up of intermediate columns
+        // ACC(0..63) = gate, ACC(64..127) = up of intermediate columns
         // j = 128 nt + 64 wg + i.
         float amax = 0.f;
         if (ok) {
 #pragma unroll
           for (int i = 0; i < 64; ++i) {
-            float gt = acc[i], up = acc[64 + i];
+            float gt = ACC(i), up = ACC(64 + i);
             if (clamp) {
               gt = fminf(gt, limit);
               up = fminf(fmaxf(up, -limit), limit);
             }
             const float a = silu_mul(gt, up);
-            acc[i] = a;
+            ACC(i) = a;
             amax = fmaxf(amax, fabsf(a));
           }
         }
@@ -389,8 +398,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
             uint32_t pk[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-              const float* a4 = acc + 32 * v + 4 * u;
-              pk[u] = pack4_e4m3(a4[0] * s, a4[1] * s, a4[2] * s, a4[3] * s);
+              const int i0 = 32 * v + 4 * u;
+              pk[u] = pack4_e4m3(ACC(i0) * s, ACC(i0 + 1) * s, ACC(i0 + 2) * s, ACC(i0 + 3) * s);
             }
             st_global_v8(dst + 32 * v, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
           }
@@ -408,10 +417,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
 #pragma unroll
           for (int v = 0; v < 16; ++v) {
             if (col0 + 8 * v < args.H) {
-              const float* a8 = acc + 8 * v;
-              st_global_v8(dst + 8 * v, __float_as_uint(a8[0] * wgt), __float_as_uint(a8[1] * wgt),
-                           __float_as_uint(a8[2] * wgt), __float_as_uint(a8[3] * wgt), __float_as_uint(a8[4] * wgt),
-                           __float_as_uint(a8[5] * wgt), __float_as_uint(a8[6] * wgt), __float_as_uint(a8[7] * wgt));
+              const float2 w2 = make_float2(wgt, wgt);
+              const float2 p0 = __fmul2_rn(acc2[4 * v], w2), p1 = __fmul2_rn(acc2[4 * v + 1], w2);
+              const float2 p2 = __fmul2_rn(acc2[4 * v + 2], w2), p3 = __fmul2_rn(acc2[4 * v + 3], w2);
+              st_global_v8(dst + 8 * v, __float_as_uint(p0.x), __float_as_uint(p0.y), __float_as_uint(p1.x),
+                           __float_as_uint(p1.y), __float_as_uint(p2.x), __float_as_uint(p2.y), __float_as_uint(p3.x),
+                           __float_as_uint(p3.y));
             }
           }
         }
