@@ -121,7 +121,7 @@ bool ws_layout(int fmt, int T, int H, int I, int E, int K, WsLayout* out) {
   p.counts = take(4ull * E);
   p.offsets = take(4ull * (E + 1));
   p.padded_offsets = take(4ull * (E + 1));
-  p.tiles = take(4ull * (kTilesHdr + E + 1));
+  p.tiles = take(4ull * (tiles_expert_of(E) + M / kBlockM));
   p.perm = take(4ull * S);
   p.inv = take(4ull * S);
   p.row_slot = take(4ull * M);
@@ -266,8 +266,14 @@ moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, cons
            cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) == cudaSuccess;
   };
   if (!mark(0)) return MOE_ERR_CUDA;
-  if (launch_route(topk_idx, L.S, E, L, ws, st) != cudaSuccess || !mark(1)) return MOE_ERR_CUDA;
-  if (launch_quant(hidden, T, H, K, L, ws, st) != cudaSuccess || !mark(2)) return MOE_ERR_CUDA;
+  if (L.S <= kFusedRouteQuantSlots) {
+    // One launch for both (the quant stage then has zero length).
+    if (launch_route_quant_small(topk_idx, hidden, T, H, E, K, L, ws, st) != cudaSuccess || !mark(1) || !mark(2))
+      return MOE_ERR_CUDA;
+  } else {
+    if (launch_route(topk_idx, L.S, E, L, ws, st) != cudaSuccess || !mark(1)) return MOE_ERR_CUDA;
+    if (launch_quant(hidden, T, H, K, L, ws, st) != cudaSuccess || !mark(2)) return MOE_ERR_CUDA;
+  }
 
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));

@@ -11,6 +11,7 @@
 #include <cuda_bf16.h>
 
 #include "moe_internal.cuh"
+#include "ptx.cuh"
 
 namespace bsmoe {
 
@@ -23,6 +24,8 @@ combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ inv, int
                __nv_bfloat16* __restrict__ out) {
   const int t = blockIdx.x;
   __shared__ int rows[kMaxTopK];
+  pdl_wait();  // y comes from GEMM2
+  pdl_launch_dependents();
   if (threadIdx.x < K) rows[threadIdx.x] = __ldg(inv + static_cast<size_t>(t) * K + threadIdx.x);
   __syncthreads();
   for (int c = (blockIdx.y * kCombineThreads + threadIdx.x) * 8; c < H; c += gridDim.y * kCombineThreads * 8) {
@@ -46,8 +49,8 @@ combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ inv, int
 
 cudaError_t launch_combine(const float* y, const int32_t* inv, int T, int H, int K, void* out, cudaStream_t st) {
   const int ygrid = ceil_div(H, kCombineThreads * 8);
-  combine_kernel<<<dim3(T, ygrid), kCombineThreads, 0, st>>>(y, inv, H, K, reinterpret_cast<__nv_bfloat16*>(out));
-  return cudaGetLastError();
+  return launch_kernel(true, combine_kernel, dim3(T, ygrid), kCombineThreads, 0, st, y, inv, H, K,
+                       reinterpret_cast<__nv_bfloat16*>(out));
 }
 
 }  // namespace bsmoe

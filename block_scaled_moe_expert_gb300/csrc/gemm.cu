@@ -86,15 +86,13 @@ struct TileCoord {
 
 // idx -> (expert, m tile, n tile). Tiles are ordered expert-major, then by n
 // tile, with the expert's m tiles fastest, so CTAs running at the same time
-// share weight tiles through L2.
+// share weight tiles through L2. Expert e owns idx in
+// [NT * mt_off[e], NT * mt_off[e + 1]), so idx / NT is one of e's global
+// m-tiles and the routing kernel's expert_of table gives e in one load.
 __device__ __forceinline__ TileCoord decode_tile(int idx, int E, int NT, const int32_t* __restrict__ mt_off,
                                                  const int32_t* __restrict__ counts,
                                                  const int32_t* __restrict__ padded_offsets) {
-  int lo = 0, hi = E;  // find e with NT*mt_off[e] <= idx < NT*mt_off[e+1]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (NT * __ldg(mt_off + mid) <= idx) lo = mid; else hi = mid;
-  }
+  const int lo = __ldg(mt_off + (E + 1) + idx / NT);  // expert_of follows the E + 1 offsets
   TileCoord c;
   c.e = lo;
   const int m_e = __ldg(mt_off + lo + 1) - __ldg(mt_off + lo);
@@ -149,7 +147,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
   const GemmGeom g = args.g;
   const int KB = g.KB, NT = g.NT;
   const int32_t* mt_off = args.tiles + kTilesHdr;
-  const int total_tiles = __ldg(args.tiles) * NT;
   volatile int* abort_flag = &sm.abort_flag;
 
   if (tid == 0) {
@@ -176,6 +173,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = sm.tmem_base;
+  // Everything above overlaps the previous kernel's tail; the tile list and
+  // the operands are written by the kernels before this one.
+  pdl_wait();
+  pdl_launch_dependents();
+  const int total_tiles = __ldg(args.tiles) * NT;
 
   if (warp < kEpiWarp0) {
    regs_dec<56>();
@@ -445,8 +447,7 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const GemmA
   const int smem = static_cast<int>(sizeof(Smem)) + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<num_sms, kThreads, smem, st>>>(ta, tb, args);
-  return cudaGetLastError();
+  return launch_kernel(true, kern, num_sms, kThreads, smem, st, ta, tb, args);
 }
 
 }  // namespace

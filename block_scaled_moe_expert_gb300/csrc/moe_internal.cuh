@@ -51,12 +51,39 @@ struct WsLayout {
 int route_chunks(int S);
 bool ws_layout(int fmt, int T, int H, int I, int E, int K, WsLayout* out);
 
-// Offsets inside the int32 "tiles" region.
-constexpr int kTilesHdr = 16;  // [0] = number of m-tiles; [16 + e] = m-tile offset of expert e (E+1)
+// Offsets inside the int32 "tiles" region: [0] = number of m-tiles;
+// [kTilesHdr + e] = m-tile offset of expert e (E + 1 entries);
+// [tiles_expert_of(E) + g] = expert owning global m-tile g (one per m-tile).
+constexpr int kTilesHdr = 16;
+__host__ __device__ constexpr int tiles_expert_of(int E) { return kTilesHdr + E + 1; }
+
+// Launches `kern` on `st`. With `dependent`, the launch may begin while the
+// preceding kernel in the stream is still running (programmatic stream
+// serialization); every kernel of the forward therefore calls pdl_wait()
+// before it touches memory that an earlier kernel writes or reads.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(bool dependent, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
 
 // ---------------------------------------------------------------- launches
 cudaError_t launch_route(const int32_t* topk_idx, int S, int E, const WsLayout& L, uint8_t* ws, cudaStream_t st);
 cudaError_t launch_quant(const void* hidden, int T, int H, int K, const WsLayout& L, uint8_t* ws, cudaStream_t st);
+// Routing + quantization in one launch, for S = T * K <= kFusedRouteQuantSlots.
+constexpr int kFusedRouteQuantSlots = 256;
+cudaError_t launch_route_quant_small(const int32_t* topk_idx, const void* hidden, int T, int H, int E, int K,
+                                     const WsLayout& L, uint8_t* ws, cudaStream_t st);
 cudaError_t launch_combine(const float* y, const int32_t* inv, int T, int H, int K, void* out, cudaStream_t st);
 cudaError_t launch_prepare(int fmt, int E, int H, int I, const void* w13, const void* w13s, const void* w2,
                            const void* w2s, uint8_t* p13, uint8_t* p2, cudaStream_t st);

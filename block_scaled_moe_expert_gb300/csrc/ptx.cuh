@@ -112,6 +112,13 @@ __device__ __forceinline__ void st_global_v8(void* p, uint32_t a, uint32_t b, ui
 }
 
 // ------------------------------------------------------------------- TMA
+// Programmatic dependent launch. wait: block until the preceding kernel in
+// the stream has completed and its memory is visible (returns at once when
+// the kernel was not launched as a dependent). launch_dependents: allow the
+// next kernel to be scheduled once every CTA of this one has issued it.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }

@@ -17,6 +17,7 @@
 
 #include "act_quant.cuh"
 #include "moe_internal.cuh"
+#include "ptx.cuh"
 
 namespace bsmoe {
 
@@ -24,30 +25,16 @@ namespace {
 
 constexpr int kQuantWarps = 8;
 
-// One CTA per token. A warp covers 256 columns (two 128-column blocks) per
-// step: each lane loads 8 bf16 (16 bytes), the 16 lanes of a half-warp reduce
-// the block's amax, and each lane stores 8 code bytes per destination row, so
-// a warp writes 256 contiguous bytes of every row it copies to.
-__global__ void __launch_bounds__(kQuantWarps * 32)
-quant_permute_kernel(const __nv_bfloat16* __restrict__ hidden, int H, int K, int Kp,
-                     const int32_t* __restrict__ inv, uint8_t* __restrict__ xq, uint32_t* __restrict__ xsf) {
-  const int t = blockIdx.x;
+// Quantizes one token row and copies its bytes to the n padded rows listed
+// in `rows`. A warp covers 256 columns (two 128-column blocks) per step: each
+// lane loads 8 bf16 (16 bytes), the 16 lanes of a half-warp reduce the
+// block's amax, and each lane stores 8 code bytes per destination row, so a
+// warp writes 256 contiguous bytes of every row it copies to.
+__device__ __forceinline__ void quantize_token(const __nv_bfloat16* __restrict__ xr, int H, int Kp,
+                                               const int* rows, int n, uint8_t* __restrict__ xq,
+                                               uint32_t* __restrict__ xsf) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nblk = Kp / 128;
-  __shared__ int rows[kMaxTopK];
-  __shared__ int nrows;
-  if (threadIdx.x == 0) {
-    int n = 0;
-    for (int k = 0; k < K; ++k) {
-      const int r = __ldg(inv + static_cast<size_t>(t) * K + k);
-      if (r >= 0) rows[n++] = r;
-    }
-    nrows = n;
-  }
-  __syncthreads();
-  const int n = nrows;
-  if (n == 0) return;
-  const __nv_bfloat16* xr = hidden + static_cast<size_t>(t) * H;
   for (int c0w = warp * 256; c0w < Kp; c0w += kQuantWarps * 256) {
     const int c0 = c0w + lane * 8;
     float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -82,14 +69,198 @@ quant_permute_kernel(const __nv_bfloat16* __restrict__ hidden, int H, int K, int
   }
 }
 
+// One CTA per token: gathers the token's valid slots from inv (in ascending
+// k) and quantizes the row into each of their padded rows.
+__global__ void __launch_bounds__(kQuantWarps * 32)
+quant_permute_kernel(const __nv_bfloat16* __restrict__ hidden, int H, int K, int Kp,
+                     const int32_t* __restrict__ inv, uint8_t* __restrict__ xq, uint32_t* __restrict__ xsf) {
+  const int t = blockIdx.x;
+  __shared__ int rows[kMaxTopK];
+  __shared__ int nrows;
+  pdl_wait();  // inv comes from the routing kernel
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    int n = 0;
+    for (int k = 0; k < K; ++k) {
+      const int r = __ldg(inv + static_cast<size_t>(t) * K + k);
+      if (r >= 0) rows[n++] = r;
+    }
+    nrows = n;
+  }
+  __syncthreads();
+  if (nrows == 0) return;
+  quantize_token(hidden + static_cast<size_t>(t) * H, H, Kp, rows, nrows, xq, xsf);
+}
+
+// ---------------------------------------------------------------------------
+// Small batches (T * K <= kFusedRouteQuantSlots): routing and quantization in
+// one launch. Every CTA (one per token) reads all S expert ids and computes
+// the complete routing in shared memory: the per-expert counts, their
+// exclusive scans (offsets, padded group starts, m-tile offsets) and each
+// slot's stable rank (the number of earlier slots with the same key), which
+// gives exactly the counting sort of the routing kernel. CTA 0 writes the
+// routing arrays; every CTA quantizes its own token into its rows.
+
+constexpr int kScanPer = 4;  // entries per thread in the (E + 1)-entry scans: 256 x 4 >= kMaxExperts + 1
+
+__device__ __forceinline__ int warp_incl_scan(int x) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  return x;
+}
+
+__global__ void __launch_bounds__(kQuantWarps * 32)
+route_quant_small_kernel(const int32_t* __restrict__ idx, const __nv_bfloat16* __restrict__ hidden, int S, int E,
+                         int K, int H, int Kp, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                         int32_t* __restrict__ padded_offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+                         int32_t* __restrict__ row_slot, int32_t* __restrict__ tiles, uint32_t* __restrict__ status,
+                         uint8_t* __restrict__ xq, uint32_t* __restrict__ xsf) {
+  constexpr int kThreads = kQuantWarps * 32;
+  __shared__ int key[kFusedRouteQuantSlots];
+  __shared__ int rank[kFusedRouteQuantSlots];
+  __shared__ int cnt[kMaxExperts + 1];
+  __shared__ int off[kMaxExperts + 1];
+  __shared__ int pad[kMaxExperts + 1];
+  __shared__ int mts[kMaxExperts + 1];
+  __shared__ int wsum[3][kQuantWarps];
+  __shared__ int rows[kMaxTopK];
+  __shared__ int nrows;
+  __shared__ int bad;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, t = blockIdx.x;
+  pdl_wait();
+  pdl_launch_dependents();
+  if (tid == 0) bad = 0;
+  for (int e = tid; e <= E; e += kThreads) cnt[e] = 0;
+  __syncthreads();
+  for (int s = tid; s < S; s += kThreads) {
+    const int v = __ldg(idx + s);
+    const int k = (v >= 0 && v < E) ? v : E;
+    if (v != -1 && k == E) bad = 1;
+    key[s] = k;
+    atomicAdd(&cnt[k], 1);
+  }
+  __syncthreads();
+
+  // Exclusive scans over the E + 1 keys of: counts, counts padded to the
+  // group alignment, m-tiles. Thread i owns entries [kScanPer i, kScanPer i + kScanPer).
+  {
+    int c[kScanPer], a[3] = {0, 0, 0};
+#pragma unroll
+    for (int j = 0; j < kScanPer; ++j) {
+      const int e = tid * kScanPer + j;
+      c[j] = (e < E) ? cnt[e] : 0;  // the skipped key E takes no rows
+      a[0] += c[j];
+      a[1] += (c[j] + kRowAlign - 1) / kRowAlign * kRowAlign;
+      a[2] += (c[j] + kBlockM - 1) / kBlockM;
+    }
+    int inc[3];
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      inc[q] = warp_incl_scan(a[q]);
+      if (lane == 31) wsum[q][warp] = inc[q];
+    }
+    __syncthreads();
+    int base[3];
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      int b = 0;
+      for (int w = 0; w < warp; ++w) b += wsum[q][w];
+      base[q] = b + inc[q] - a[q];
+    }
+#pragma unroll
+    for (int j = 0; j < kScanPer; ++j) {
+      const int e = tid * kScanPer + j;
+      if (e <= E) {
+        off[e] = base[0];
+        pad[e] = base[1];
+        mts[e] = base[2];
+      }
+      base[0] += c[j];
+      base[1] += (c[j] + kRowAlign - 1) / kRowAlign * kRowAlign;
+      base[2] += (c[j] + kBlockM - 1) / kBlockM;
+    }
+  }
+  // Stable rank of every slot among the slots with the same key.
+  for (int s = warp; s < S; s += kQuantWarps) {
+    const int k = key[s];
+    int c = 0;
+    for (int j = lane; j < s; j += 32) c += (key[j] == k);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    if (lane == 0) rank[s] = c;
+  }
+  __syncthreads();
+
+  if (t == 0) {
+    if (tid == 0) {
+      *status = bad ? MOE_DEV_BAD_EXPERT_ID : 0u;
+      offsets[E] = off[E];
+      padded_offsets[E] = pad[E];
+      tiles[0] = mts[E];
+      tiles[kTilesHdr + E] = mts[E];
+    }
+    for (int e = tid; e < E; e += kThreads) {
+      counts[e] = cnt[e];
+      offsets[e] = off[e];
+      padded_offsets[e] = pad[e];
+      tiles[kTilesHdr + e] = mts[e];
+    }
+    for (int s = tid; s < S; s += kThreads) {
+      const int k = key[s];
+      perm[off[k] + rank[s]] = s;  // skipped slots: key E, after every group
+      if (k < E) {
+        const int row = pad[k] + rank[s];
+        inv[s] = row;
+        row_slot[row] = s;
+      } else {
+        inv[s] = -1;
+      }
+    }
+    int32_t* expert_of = tiles + tiles_expert_of(E);
+    for (int e = warp; e < E; e += kQuantWarps) {
+      for (int g = mts[e] + lane; g < mts[e + 1]; g += 32) expert_of[g] = e;
+      for (int r = pad[e] + cnt[e] + lane; r < pad[e + 1]; r += 32) row_slot[r] = -1;  // padding rows
+    }
+  }
+
+  if (tid == 0) {
+    int n = 0;
+    for (int k = 0; k < K; ++k) {
+      const int s = t * K + k;
+      if (key[s] < E) rows[n++] = pad[key[s]] + rank[s];
+    }
+    nrows = n;
+  }
+  __syncthreads();
+  if (nrows == 0) return;
+  quantize_token(hidden + static_cast<size_t>(t) * H, H, Kp, rows, nrows, xq, xsf);
+}
+
 }  // namespace
 
 cudaError_t launch_quant(const void* hidden, int T, int H, int K, const WsLayout& L, uint8_t* ws, cudaStream_t st) {
   const moe_workspace_layout& p = L.pub;
-  quant_permute_kernel<<<T, kQuantWarps * 32, 0, st>>>(
-      reinterpret_cast<const __nv_bfloat16*>(hidden), H, K, p.xq_cols, reinterpret_cast<const int32_t*>(ws + p.inv),
-      ws + p.xq, reinterpret_cast<uint32_t*>(ws + p.xsf));
-  return cudaGetLastError();
+  return launch_kernel(true, quant_permute_kernel, T, kQuantWarps * 32, 0, st,
+                       reinterpret_cast<const __nv_bfloat16*>(hidden), H, K, p.xq_cols,
+                       reinterpret_cast<const int32_t*>(ws + p.inv), ws + p.xq, reinterpret_cast<uint32_t*>(ws + p.xsf));
+}
+
+cudaError_t launch_route_quant_small(const int32_t* topk_idx, const void* hidden, int T, int H, int E, int K,
+                                     const WsLayout& L, uint8_t* ws, cudaStream_t st) {
+  const moe_workspace_layout& p = L.pub;
+  // The first kernel of the forward is an ordinary launch: it follows
+  // whatever the caller queued on the stream.
+  return launch_kernel(false, route_quant_small_kernel, T, kQuantWarps * 32, 0, st, topk_idx,
+                       reinterpret_cast<const __nv_bfloat16*>(hidden), T * K, E, K, H, p.xq_cols,
+                       reinterpret_cast<int32_t*>(ws + p.counts), reinterpret_cast<int32_t*>(ws + p.offsets),
+                       reinterpret_cast<int32_t*>(ws + p.padded_offsets), reinterpret_cast<int32_t*>(ws + p.perm),
+                       reinterpret_cast<int32_t*>(ws + p.inv), reinterpret_cast<int32_t*>(ws + p.row_slot),
+                       reinterpret_cast<int32_t*>(ws + p.tiles), reinterpret_cast<uint32_t*>(ws + p.status),
+                       ws + p.xq, reinterpret_cast<uint32_t*>(ws + p.xsf));
 }
 
 }  // namespace bsmoe

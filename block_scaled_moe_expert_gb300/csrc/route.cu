@@ -14,6 +14,7 @@
 // own warp), which is exactly the stable order. No data atomics are used:
 // the result is deterministic.
 #include "moe_internal.cuh"
+#include "ptx.cuh"
 
 namespace bsmoe {
 
@@ -28,6 +29,14 @@ __device__ __forceinline__ int slot_key(const int32_t* idx, int s, int E, uint32
   if (v >= 0 && v < E) return v;
   if (v != -1 && status != nullptr) atomicOr(status, MOE_DEV_BAD_EXPERT_ID);
   return E;
+}
+
+// expert_of[g] = e for every m-tile g of expert e (m-tile offsets in s_mt,
+// E + 1 entries): lets the GEMMs find a tile's expert with one load.
+__device__ __forceinline__ void write_expert_of(int E, const int* s_mt, int32_t* expert_of) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  for (int e = warp; e < E; e += nwarps)
+    for (int g = s_mt[e] + lane; g < s_mt[e + 1]; g += 32) expert_of[g] = e;
 }
 
 // Block-wide exclusive scan of one int per thread (1024 threads).
@@ -68,8 +77,11 @@ route_kernel(const int32_t* __restrict__ idx, int S, int E, int M, int32_t* __re
   __shared__ int tot[3];
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_pad[kMaxExperts + 1];
+  __shared__ int s_mt[kMaxExperts + 1];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int stride = E + 1;
+  pdl_wait();
+  pdl_launch_dependents();
   // The status word reflects the most recent forward on this workspace.
   if (tid == 0) *status = 0u;
   for (int i = tid; i < kWarps * stride; i += kThreads) hist[i] = 0;
@@ -115,6 +127,7 @@ route_kernel(const int32_t* __restrict__ idx, int S, int E, int M, int32_t* __re
     tiles[kTilesHdr + tid] = mts;
     s_off[tid] = off;
     s_pad[tid] = pad;
+    s_mt[tid] = mts;
   }
   if (tid == 0) {
     offsets[E] = tot[0];
@@ -123,8 +136,10 @@ route_kernel(const int32_t* __restrict__ idx, int S, int E, int M, int32_t* __re
     tiles[0] = tot[2];
     s_off[E] = tot[0];
     s_pad[E] = tot[1];
+    s_mt[E] = tot[2];
   }
   __syncthreads();
+  write_expert_of(E, s_mt, tiles + tiles_expert_of(E));
 
   // Pass 2: scatter.
   for (int base = beg; base < end; base += 32) {
@@ -173,6 +188,8 @@ constexpr int kChunkWarps = 8;
 __global__ void __launch_bounds__(kChunkWarps * 32)
 route_hist_kernel(const int32_t* __restrict__ idx, int S, int E, int32_t* __restrict__ chunk_hist) {
   extern __shared__ int h[];  // [E + 1]
+  pdl_wait();
+  pdl_launch_dependents();
   for (int i = threadIdx.x; i <= E; i += blockDim.x) h[i] = 0;
   __syncthreads();
   const int beg = blockIdx.x * kChunk, end = min(S, beg + kChunk);
@@ -189,7 +206,10 @@ route_scan_kernel(int E, int G, int32_t* __restrict__ chunk_hist, int32_t* __res
   __shared__ int tot[3];
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_pad[kMaxExperts + 1];
+  __shared__ int s_mt[kMaxExperts + 1];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();
+  pdl_launch_dependents();
   // The status word reflects the most recent forward; the scatter kernel
   // raises the invalid-id flag after this.
   if (tid == 0) *status = 0u;
@@ -215,6 +235,7 @@ route_scan_kernel(int E, int G, int32_t* __restrict__ chunk_hist, int32_t* __res
     tiles[kTilesHdr + tid] = mts;
     s_off[tid] = off;
     s_pad[tid] = pad;
+    s_mt[tid] = mts;
   }
   if (tid == 0) {
     offsets[E] = tot[0];
@@ -223,8 +244,10 @@ route_scan_kernel(int E, int G, int32_t* __restrict__ chunk_hist, int32_t* __res
     tiles[0] = tot[2];
     s_off[E] = tot[0];
     s_pad[E] = tot[1];
+    s_mt[E] = tot[2];
   }
   __syncthreads();
+  write_expert_of(E, s_mt, tiles + tiles_expert_of(E));
   for (int e = warp; e < E; e += kWarps) {
     const int lo = s_pad[e] + (s_off[e + 1] - s_off[e]);
     const int hi = s_pad[e + 1];
@@ -243,6 +266,8 @@ route_scatter_kernel(const int32_t* __restrict__ idx, int S, int E, const int32_
   int* s_off = smem + kChunkWarps * stride;  // [E + 1]
   int* s_pad = s_off + stride;               // [E + 1]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();
+  pdl_launch_dependents();
   for (int i = tid; i < kChunkWarps * stride; i += blockDim.x) hist[i] = 0;
   for (int i = tid; i <= E; i += blockDim.x) {
     s_off[i] = offsets[i];
@@ -308,30 +333,33 @@ cudaError_t launch_route(const int32_t* topk_idx, int S, int E, const WsLayout& 
   if (G > 0) {
     int32_t* chunk_hist = reinterpret_cast<int32_t*>(ws + L.route_scratch);
     uint32_t* status = reinterpret_cast<uint32_t*>(ws + p.status);
-    route_hist_kernel<<<G, kChunkWarps * 32, sizeof(int) * (E + 1), st>>>(topk_idx, S, E, chunk_hist);
-    route_scan_kernel<<<1, kThreads, 0, st>>>(E, G, chunk_hist, reinterpret_cast<int32_t*>(ws + p.counts),
-                                              reinterpret_cast<int32_t*>(ws + p.offsets),
-                                              reinterpret_cast<int32_t*>(ws + p.padded_offsets),
-                                              reinterpret_cast<int32_t*>(ws + p.row_slot),
-                                              reinterpret_cast<int32_t*>(ws + p.tiles), status);
+    cudaError_t e = launch_kernel(false, route_hist_kernel, G, kChunkWarps * 32, sizeof(int) * (E + 1), st,
+                                  topk_idx, S, E, chunk_hist);
+    if (e != cudaSuccess) return e;
+    e = launch_kernel(true, route_scan_kernel, 1, kThreads, 0, st, E, G, chunk_hist,
+                      reinterpret_cast<int32_t*>(ws + p.counts), reinterpret_cast<int32_t*>(ws + p.offsets),
+                      reinterpret_cast<int32_t*>(ws + p.padded_offsets), reinterpret_cast<int32_t*>(ws + p.row_slot),
+                      reinterpret_cast<int32_t*>(ws + p.tiles), status);
+    if (e != cudaSuccess) return e;
     const size_t smem = sizeof(int) * (kChunkWarps + 2) * (E + 1);
-    route_scatter_kernel<<<G, kChunkWarps * 32, smem, st>>>(
-        topk_idx, S, E, chunk_hist, reinterpret_cast<const int32_t*>(ws + p.offsets),
-        reinterpret_cast<const int32_t*>(ws + p.padded_offsets), reinterpret_cast<int32_t*>(ws + p.perm),
-        reinterpret_cast<int32_t*>(ws + p.inv), reinterpret_cast<int32_t*>(ws + p.row_slot), status);
-    return cudaGetLastError();
+    return launch_kernel(true, route_scatter_kernel, G, kChunkWarps * 32, smem, st, topk_idx, S, E,
+                         static_cast<const int32_t*>(chunk_hist), reinterpret_cast<const int32_t*>(ws + p.offsets),
+                         reinterpret_cast<const int32_t*>(ws + p.padded_offsets),
+                         reinterpret_cast<int32_t*>(ws + p.perm), reinterpret_cast<int32_t*>(ws + p.inv),
+                         reinterpret_cast<int32_t*>(ws + p.row_slot), status);
   }
   const size_t smem = sizeof(int) * kWarps * (E + 1);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  route_kernel<<<1, kThreads, smem, st>>>(
-      topk_idx, S, E, L.M, reinterpret_cast<int32_t*>(ws + p.counts), reinterpret_cast<int32_t*>(ws + p.offsets),
-      reinterpret_cast<int32_t*>(ws + p.padded_offsets), reinterpret_cast<int32_t*>(ws + p.perm),
-      reinterpret_cast<int32_t*>(ws + p.inv), reinterpret_cast<int32_t*>(ws + p.row_slot),
-      reinterpret_cast<int32_t*>(ws + p.tiles), reinterpret_cast<uint32_t*>(ws + p.status));
-  return cudaGetLastError();
+  // The first kernel of the forward is an ordinary launch: it follows
+  // whatever the caller queued on the stream.
+  return launch_kernel(false, route_kernel, 1, kThreads, smem, st, topk_idx, S, E, L.M,
+                       reinterpret_cast<int32_t*>(ws + p.counts), reinterpret_cast<int32_t*>(ws + p.offsets),
+                       reinterpret_cast<int32_t*>(ws + p.padded_offsets), reinterpret_cast<int32_t*>(ws + p.perm),
+                       reinterpret_cast<int32_t*>(ws + p.inv), reinterpret_cast<int32_t*>(ws + p.row_slot),
+                       reinterpret_cast<int32_t*>(ws + p.tiles), reinterpret_cast<uint32_t*>(ws + p.status));
 }
 
 }  // namespace bsmoe

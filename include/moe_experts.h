@@ -210,6 +210,9 @@ moe_status moe_get_device_status(void* workspace, void* stream, uint32_t* flags)
  *   perm [S] (sorted position -> slot, skipped slots last);
  *   inv [S] (slot -> padded row, -1 if skipped);
  *   row_slot [M] (padded row -> slot, -1 for padding rows);
+ *   tiles [16 + (E+1) + M/128]: [0] number of 128-row m-tiles, [16 + e]
+ *     first m-tile of expert e (E+1 entries), then the expert owning each
+ *     m-tile (GEMM work list);
  *   xq u8 [M, xq_cols] (e4m3 hidden rows in grouped order);
  *   xsf u32 (activation scale words, see below);
  *   act u8 [M, act_cols] (e4m3 SwiGLU output), asf u32 likewise;

@@ -50,6 +50,20 @@ def test_deterministic_and_batch_invariant():
     assert (out[wl.T:].view(torch.int16) == 0).all()
 
 
+def test_small_batch_kernel_matches_the_general_path():
+    """T*K <= 256 routes and quantizes in one fused kernel; the same tokens
+    inside a larger batch take the separate kernels. Same bits either way."""
+    wl = W.Workload("fused_vs_split", 120, 256, 256, 8, 2, "fp8", "zipf_sigmoid", seed=41, skip_frac=0.1)
+    r = P.run_cuda(wl)
+    extra = 20
+    hid = torch.cat([r["hidden"], r["hidden"][:extra]])
+    idx = torch.cat([r["idx"], r["idx"][:extra]])
+    w = torch.cat([r["w"], r["w"][:extra]])
+    out = P.B.experts_forward(hid, idx, w, r["prepared"])
+    assert torch.equal(out[:wl.T].view(torch.int16), r["out"].view(torch.int16))
+    P.assert_close(r["out"], P.oracle_out(r["hidden"], r["idx"], r["w"], r["weights"], None), "fused")
+
+
 def test_all_skipped_gives_positive_zero():
     wl = W.scaled(CASES[1], T=50)
     idx = torch.full((wl.T, wl.K), -1, dtype=torch.int32, device="cuda")

@@ -28,6 +28,14 @@ def _check_route_quant(wl, r):
     assert (inv == ref["inv"]).all()
     M = int(ref["padded_offsets"][E])
     assert (get("row_slot", M) == ref["row_slot"]).all()
+    # GEMM work list: m-tile offsets per expert and the expert of each m-tile
+    mtiles = -(-ref["counts"] // 128)
+    mt_off = np.concatenate([[0], np.cumsum(mtiles)])
+    n_mt = int(mt_off[-1])
+    tiles = get("tiles", 16 + E + 1 + n_mt)
+    assert tiles[0] == n_mt
+    assert (tiles[16:16 + E + 1] == mt_off).all()
+    assert (tiles[16 + E + 1:] == np.repeat(np.arange(E), mtiles)).all()
 
     codes, exps = P.OM.quantize_hidden(P.bits_of(r["hidden"]))
     valid = np.flatnonzero(ref["inv"] >= 0)
@@ -48,6 +56,10 @@ CASES = [
     P.W.scaled(P.W.WORKLOADS["dsv3_decode_fp8"], T=512, H=256, I=128),
     P.W.scaled(P.W.WORKLOADS["gptoss_fp8xfp4"], T=333, H=2880, I=128, E=16),
     P.W.scaled(P.W.WORKLOADS["dsv3_decode_fp4_T1"], H=512, I=256),
+    # 256 slots: the fused small-batch routing + quantization kernel; 264: the
+    # separate routing and quantization kernels
+    P.W.scaled(P.W.WORKLOADS["dsv3_decode_fp8"], T=32, H=256, I=128),
+    P.W.scaled(P.W.WORKLOADS["dsv3_decode_fp8"], T=33, H=256, I=128),
     # more than 8192 slots: the multi-CTA routing path (5 and 17 chunks)
     P.W.scaled(P.W.WORKLOADS["dsv3_decode_fp8"], T=1250, H=256, I=128),
     P.W.scaled(P.W.WORKLOADS["gptoss_fp8xfp4"], T=8500, H=256, I=128, E=128),
@@ -108,3 +120,18 @@ def test_quantizer_exhaustive_bf16_sweep():
     w = torch.ones(T, 1, dtype=torch.float32, device="cuda")
     r = P.run_cuda(wl, hidden=hidden, idx=idx, w=w)
     _check_route_quant(wl, r)
+
+
+@pytest.mark.parametrize("T", [9, 70])
+def test_duplicate_ids_in_one_token(T):
+    """A token may name the same expert twice: each pair is routed on its own
+    (fused small-batch kernel at T=9, separate kernels at T=70)."""
+    wl = P.W.Workload("dups", T, 256, 128, 8, 4, "fp8", "softmax", seed=55)
+    idx, w = P.W.make_routing(wl, "cuda")
+    idx[0] = torch.tensor([3, 3, 3, 5], dtype=torch.int32)
+    idx[T - 1] = torch.tensor([-1, 2, 2, -1], dtype=torch.int32)
+    idx[T // 2] = -1
+    r = P.run_cuda(wl, idx=idx, w=w)
+    _check_route_quant(wl, r)
+    ref = P.oracle_out(r["hidden"], r["idx"], r["w"], r["weights"], None)
+    P.assert_close(r["out"], ref, f"dups T={T}")
