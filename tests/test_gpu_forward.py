@@ -22,6 +22,10 @@ CASES = [
     W.Workload("fp4_gptoss_like", 300, 2880, 2880, 8, 4, "fp4", "softmax", seed=15, logit_std=1.5,
                swiglu_limit=7.0),
     W.Workload("fp4_ragged_h", 130, 320, 192, 5, 3, "fp4", "softmax", seed=16, swiglu_limit=0.2),
+    # FP4 with few pairs per expert (mostly one partly filled m-tile each)
+    W.Workload("fp4_small_ragged", 40, 320, 192, 8, 3, "fp4", "softmax", seed=17, swiglu_limit=0.25),
+    W.Workload("fp4_small_zipf", 64, 512, 256, 32, 8, "fp4", "zipf_sigmoid", seed=18, skip_frac=0.05),
+    W.Workload("fp4_small_T1", 1, 512, 384, 16, 4, "fp4", "softmax", seed=19),
 ]
 
 
@@ -128,3 +132,19 @@ def test_refusals():
                                wl.K, 0, r["prepared"].w13_prep.data_ptr(), r["prepared"].w2_prep.data_ptr(),
                                float("nan"), r["ws"].data_ptr(), r["ws"].numel(), r["out"].data_ptr(), None)
     assert st == 4  # MOE_ERR_DEVICE_MISMATCH: a host pointer
+
+
+def test_fp4_token_outputs_do_not_depend_on_the_batch():
+    """8 tokens alone and inside a 68-token batch (other experts' m-tiles, more
+    rows in the same tiles): the same bits, and both match the oracle."""
+    wl = W.Workload("fp4_batch", 8, 512, 256, 8, 4, "fp4", "softmax", seed=23)
+    r = P.run_cuda(wl)
+    ref = P.oracle_out(r["hidden"], r["idx"], r["w"], r["weights"], None)
+    P.assert_close(r["out"], ref, "8 tokens")
+    extra = 60
+    g = torch.Generator(device="cuda").manual_seed(5)
+    hid = torch.cat([r["hidden"], (torch.randn(extra, wl.H, generator=g, device="cuda")).to(torch.bfloat16)])
+    idx = torch.cat([r["idx"], torch.randint(0, wl.E, (extra, wl.K), generator=g, device="cuda", dtype=torch.int32)])
+    w = torch.cat([r["w"], torch.rand(extra, wl.K, generator=g, device="cuda")])
+    out = P.B.experts_forward(hid, idx, w, r["prepared"])
+    assert torch.equal(out[:wl.T].view(torch.int16), r["out"].view(torch.int16))
