@@ -46,6 +46,7 @@ _SIGS = {
     "moe_prepared_w2_bytes": (_sz, [_int, _int, _int, _int]),
     "moe_workspace_bytes": (_sz, [_int, _int, _int, _int, _int, _int]),
     "moe_prepare_weights": (_int, [_int, _int, _int, _int, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _sz, _vp]),
+    "moe_prepare_weights_transposed": (_int, [_int, _int, _int, _int, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _sz, _vp]),
     "moe_experts_forward": (_int, [_vp, _vp, _vp, _int, _int, _int, _int, _int, _int, _vp, _vp, _f32, _vp, _sz,
                                    _vp, _vp]),
     "moe_experts_forward_timed": (_int, [_vp, _vp, _vp, _int, _int, _int, _int, _int, _int, _vp, _vp, _f32, _vp,
@@ -122,8 +123,10 @@ class PreparedWeights:
         self.w13_prep, self.w2_prep = w13_prep, w2_prep
 
 
-def prepare_weights(weights):
-    """weights: dict(fmt, E, H, I, w13, w13_scale, w2, w2_scale) of CUDA tensors."""
+def prepare_weights(weights, transposed=False):
+    """weights: dict(fmt, E, H, I, w13, w13_scale, w2, w2_scale) of CUDA tensors,
+    K-major ([E, N, K]) or, with transposed=True, N-major ([E, K, N]; see
+    moe_prepare_weights_transposed for the exact shapes)."""
     fmt, E, H, I = weights["fmt"], weights["E"], weights["H"], weights["I"]
     ts = [weights[k].contiguous() for k in ("w13", "w13_scale", "w2", "w2_scale")]
     _same_device(*ts)
@@ -135,8 +138,8 @@ def prepare_weights(weights):
     dev = ts[0].device
     p13 = torch.empty(n13, dtype=torch.uint8, device=dev)
     p2 = torch.empty(n2, dtype=torch.uint8, device=dev)
-    _check(L.moe_prepare_weights(FMT[fmt], E, H, I, *[_ptr(t) for t in ts], _ptr(p13), n13, _ptr(p2), n2,
-                                 _stream()), "moe_prepare_weights")
+    fn = "moe_prepare_weights_transposed" if transposed else "moe_prepare_weights"
+    _check(getattr(L, fn)(FMT[fmt], E, H, I, *[_ptr(t) for t in ts], _ptr(p13), n13, _ptr(p2), n2, _stream()), fn)
     return PreparedWeights(fmt, E, H, I, p13, p2)
 
 

@@ -192,9 +192,13 @@ moe_status moe_query_workspace_layout(int fmt, int T, int H, int I, int E, int K
   return MOE_OK;
 }
 
-moe_status moe_prepare_weights(int fmt, int E, int H, int I, const void* w13, const void* w13_scale, const void* w2,
-                               const void* w2_scale, void* w13_prep, size_t w13_prep_bytes, void* w2_prep,
-                               size_t w2_prep_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+moe_status prepare_impl(bool transposed, int fmt, int E, int H, int I, const void* w13, const void* w13_scale,
+                        const void* w2, const void* w2_scale, void* w13_prep, size_t w13_prep_bytes, void* w2_prep,
+                        size_t w2_prep_bytes, void* stream) {
   if (!shape_ok(fmt, H, I, E)) return MOE_ERR_UNSUPPORTED_SHAPE;
   const void* ptrs[6] = {w13, w13_scale, w2, w2_scale, w13_prep, w2_prep};
   for (const void* p : ptrs)
@@ -208,10 +212,29 @@ moe_status moe_prepare_weights(int fmt, int E, int H, int I, const void* w13, co
   if (s != MOE_OK) return s;
   for (const void* p : ptrs)
     if ((s = check_ptr(p, d.id)) != MOE_OK) return s;
-  if (launch_prepare(fmt, E, H, I, w13, w13_scale, w2, w2_scale, static_cast<uint8_t*>(w13_prep),
+  if (launch_prepare(fmt, transposed, E, H, I, w13, w13_scale, w2, w2_scale, static_cast<uint8_t*>(w13_prep),
                      static_cast<uint8_t*>(w2_prep), static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_prepare_weights(int fmt, int E, int H, int I, const void* w13, const void* w13_scale, const void* w2,
+                               const void* w2_scale, void* w13_prep, size_t w13_prep_bytes, void* w2_prep,
+                               size_t w2_prep_bytes, void* stream) {
+  return prepare_impl(false, fmt, E, H, I, w13, w13_scale, w2, w2_scale, w13_prep, w13_prep_bytes, w2_prep,
+                      w2_prep_bytes, stream);
+}
+
+moe_status moe_prepare_weights_transposed(int fmt, int E, int H, int I, const void* w13, const void* w13_scale,
+                                          const void* w2, const void* w2_scale, void* w13_prep,
+                                          size_t w13_prep_bytes, void* w2_prep, size_t w2_prep_bytes,
+                                          void* stream) {
+  return prepare_impl(true, fmt, E, H, I, w13, w13_scale, w2, w2_scale, w13_prep, w13_prep_bytes, w2_prep,
+                      w2_prep_bytes, stream);
 }
 
 }  // extern "C"

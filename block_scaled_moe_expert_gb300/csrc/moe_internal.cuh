@@ -85,8 +85,9 @@ constexpr int kFusedRouteQuantSlots = 256;
 cudaError_t launch_route_quant_small(const int32_t* topk_idx, const void* hidden, int T, int H, int E, int K,
                                      const WsLayout& L, uint8_t* ws, cudaStream_t st);
 cudaError_t launch_combine(const float* y, const int32_t* inv, int T, int H, int K, void* out, cudaStream_t st);
-cudaError_t launch_prepare(int fmt, int E, int H, int I, const void* w13, const void* w13s, const void* w2,
-                           const void* w2s, uint8_t* p13, uint8_t* p2, cudaStream_t st);
+// transposed: the weights are stored [E][K][N] (N contiguous) instead of [E][N][K].
+cudaError_t launch_prepare(int fmt, bool transposed, int E, int H, int I, const void* w13, const void* w13s,
+                           const void* w2, const void* w2s, uint8_t* p13, uint8_t* p2, cudaStream_t st);
 
 struct GemmArgs {
   // operands

@@ -126,6 +126,26 @@ moe_status moe_prepare_weights(int fmt, int E, int H, int I, const void* w13, co
                                void* w2_prep, size_t w2_prep_bytes, void* stream);
 
 /*
+ * The same transform for expert weights stored transposed, N contiguous
+ * (the `is_transposed` storage that the experts dispatch serves with
+ * grouped_fp8_fp4_matmul_nn instead of _nt, deepgemm.py error record,
+ * lines 678-714). Writes exactly the bytes moe_prepare_weights writes for
+ * the same weights in the K-major storage, so the forward does not change.
+ *
+ * Inputs (read only, device):
+ *   MOE_W_FP8: w13 u8 [E, H, 2I], w13_scale f32 [E, H/128, 2I/128],
+ *              w2  u8 [E, I, H],  w2_scale  f32 [E, I/128, H/128];
+ *   MOE_W_FP4: w13 u8 [E, H, 2I/2] (two codes per byte along N, low nibble
+ *              = even N index), w13_scale u8 [E, H/32, 2I] (UE8M0 per 32 K
+ *              of one N column), w2 u8 [E, I, H/2], w2_scale u8 [E, I/32, H].
+ * Outputs, ownership and errors as moe_prepare_weights.
+ */
+moe_status moe_prepare_weights_transposed(int fmt, int E, int H, int I, const void* w13, const void* w13_scale,
+                                          const void* w2, const void* w2_scale, void* w13_prep,
+                                          size_t w13_prep_bytes, void* w2_prep, size_t w2_prep_bytes,
+                                          void* stream);
+
+/*
  * The experts forward:
  *   out[t, :] = bf16( sum_{k : idx[t,k] valid} w[t,k] * FFN_{idx[t,k]}(x[t, :]) )
  * summed in ascending k in fp32 (deterministic, no atomics); a token whose

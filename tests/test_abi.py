@@ -87,9 +87,11 @@ def test_argument_checks_before_any_device_call(L):
     assert L.moe_experts_forward_static(None, None, None, 4096, 7168, 2048, 8, 2, 0, None, None, nan, None,
                                         None) == 6
     assert L.moe_static_workspace_capacity() == 64 << 20
-    # prepare: null / misaligned
-    assert L.moe_prepare_weights(0, 8, 256, 128, None, None, None, None, None, 0, None, 0, None) == 1
-    assert L.moe_prepare_weights(0, 8, 256, 128, p, p, p, p, p, 1 << 30, p, 1 << 30, None) == 5
+    # prepare (both storages): null / misaligned / unsupported shape
+    for fn in (L.moe_prepare_weights, L.moe_prepare_weights_transposed):
+        assert fn(0, 8, 256, 128, None, None, None, None, None, 0, None, 0, None) == 1
+        assert fn(0, 8, 256, 128, p, p, p, p, p, 1 << 30, p, 1 << 30, None) == 5
+        assert fn(0, 8, 200, 128, p, p, p, p, p, 1 << 30, p, 1 << 30, None) == 2
 
 
 def test_python_refusals_without_gpu():
