@@ -107,9 +107,13 @@ def weight_bytes_per_expert(wl, which):
 
 
 def launches_per_forward(wl):
-    """Kernels one forward launches: routing (one kernel up to 8192 slots,
-    else histogram + scan + scatter), quantization, GEMM1, GEMM2, combine."""
-    return (1 if wl.T * wl.K <= 8192 else 3) + 4
+    """Kernels one forward launches: routing + quantization (one fused kernel
+    up to 256 slots; else one routing kernel up to 8192 slots or histogram +
+    scan + scatter, then the quantization kernel), GEMM1, GEMM2, combine."""
+    S = wl.T * wl.K
+    if S <= 256:
+        return 4
+    return (1 if S <= 8192 else 3) + 4
 
 
 def routing_stats(idx_cpu, E):
