@@ -121,7 +121,7 @@ bool ws_layout(int fmt, int T, int H, int I, int E, int K, WsLayout* out) {
   p.counts = take(4ull * E);
   p.offsets = take(4ull * (E + 1));
   p.padded_offsets = take(4ull * (E + 1));
-  p.tiles = take(4ull * (tiles_expert_of(E) + M / kBlockM));
+  p.tiles = take(4ull * tiles_ints(E, static_cast<int>(M)));
   p.perm = take(4ull * S);
   p.inv = take(4ull * S);
   p.row_slot = take(4ull * M);
@@ -274,12 +274,16 @@ moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, cons
   const GemmGeom g1 = geom_w13(H, I), g2 = geom_w2(H, I);
   const PrepLayout P1 = prep_layout(fmt, E, g1), P2 = prep_layout(fmt, E, g2);
   const bool fp4 = (fmt == MOE_W_FP4);
+  // FP4 weights with few pairs per expert: the weight-streaming decode mode
+  // of the grouped GEMMs (32-row token chunks, five weight stages).
+  const bool decode = fp4 && static_cast<long long>(L.S) <= static_cast<long long>(kDecodePairsPerExpert) * E;
+  const int a_box = decode ? kChunkRows : kBlockM;
 
   CUtensorMap ta1, tb1, ta2, tb2;
-  if (!make_tmap(&ta1, false, ws + p.xq, g1.Kp, L.M, kBlockM) ||
+  if (!make_tmap(&ta1, false, ws + p.xq, g1.Kp, L.M, a_box) ||
       !make_tmap(&tb1, fp4, static_cast<const uint8_t*>(w13_prep) + P1.codes_off, g1.Kp,
                  static_cast<uint64_t>(E) * g1.Np, kBlockN) ||
-      !make_tmap(&ta2, false, ws + p.act, g2.Kp, L.M, kBlockM) ||
+      !make_tmap(&ta2, false, ws + p.act, g2.Kp, L.M, a_box) ||
       !make_tmap(&tb2, fp4, static_cast<const uint8_t*>(w2_prep) + P2.codes_off, g2.Kp,
                  static_cast<uint64_t>(E) * g2.Np, kBlockN))
     return MOE_ERR_CUDA;
@@ -309,6 +313,7 @@ moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, cons
   a.E = E;
   a.I = I;
   a.H = H;
+  a.M = L.M;
   a.swiglu_limit = (std::isfinite(swiglu_limit) && swiglu_limit > 0.f) ? swiglu_limit : 0.f;
 
   GemmArgs a1 = a;
@@ -319,7 +324,7 @@ moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, cons
   a1.out_cols = g2.Kp;
   a1.out_blocks = g2.KB;
   a1.g = g1;
-  if (launch_gemm(fmt, true, ta1, tb1, a1, d.sms, st) != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;
+  if (launch_gemm(fmt, true, decode, ta1, tb1, a1, d.sms, st) != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;
 
   GemmArgs a2 = a;
   a2.a_sf = ws + p.asf;
@@ -327,7 +332,7 @@ moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, cons
   a2.out_y = reinterpret_cast<float*>(ws + p.y);
   a2.out_cols = H;
   a2.g = g2;
-  if (launch_gemm(fmt, false, ta2, tb2, a2, d.sms, st) != cudaSuccess || !mark(4)) return MOE_ERR_CUDA;
+  if (launch_gemm(fmt, false, decode, ta2, tb2, a2, d.sms, st) != cudaSuccess || !mark(4)) return MOE_ERR_CUDA;
 
   if (launch_combine(reinterpret_cast<const float*>(ws + p.y), reinterpret_cast<const int32_t*>(ws + p.inv), T, H,
                      K, out, st) != cudaSuccess || !mark(5))

@@ -41,11 +41,10 @@ namespace bsmoe {
 
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kThreads = 384;
 constexpr int kEpiWarp0 = 4;  // warps 4..11 are the two epilogue warpgroups
 constexpr int kEpiThreads = 256;
-constexpr uint32_t kTileABytes = kBlockM * kBlockK;  // 16 KB
+constexpr uint32_t kTileABytes = kBlockM * kBlockK;  // 16 KB: the 128 activation rows an MMA reads
 constexpr uint32_t kTileBBytes = kBlockN * kBlockK;  // 32 KB (FP4 is unpacked to 1 B/elem in smem)
 constexpr uint32_t kSfaBytes = 512;
 constexpr uint32_t kSfbBytes = 1024;
@@ -55,13 +54,30 @@ constexpr uint32_t kSwBytes = 32;       // FP8: 8 weight scales (one per 32 colu
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfTmemCol = 256;  // FP4: per stage 4 SFA + 8 SFB columns from here
 
-struct __align__(1024) Smem {
-  uint8_t a[kStages][kTileABytes];
-  uint8_t b[kStages][kTileBBytes];
-  uint8_t sfa[kStages][kSfaBytes];
-  uint8_t sfb[kStages][kSfbBytes];
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+// Pipeline shape. Tile mode: a work unit is a 128-row token tile; a stage
+// holds its 16 KB of activation rows and a 32 KB weight tile (4 stages).
+// Decode mode (FP4 weights, few pairs per expert): a work unit is a 32-row
+// token chunk and a stage loads only its 4 KB of activation rows into an
+// overlapping window: the MMA reads 128 rows from the window start, rows
+// 32-127 being whatever follows in shared memory; they only reach output
+// rows that are never stored. The 12 KB saved per stage buy a fifth weight
+// stage, i.e. 80 KB instead of 64 KB of FP4 weights in flight per SM.
+template <bool DEC>
+struct Pipe {
+  static constexpr int kStages = DEC ? 5 : 4;
+  static constexpr int kRows = DEC ? kChunkRows : kBlockM;  // activation rows loaded per stage
+  static constexpr uint32_t kAStride = kRows * kBlockK;
+  static constexpr uint32_t kARegion = kStages * kAStride + (kTileABytes - kAStride);
+};
+
+template <bool DEC>
+struct __align__(1024) SmemT {
+  uint8_t b[Pipe<DEC>::kStages][kTileBBytes];
+  uint8_t a[Pipe<DEC>::kARegion];  // stage s at s * kAStride (1024-byte aligned)
+  uint8_t sfa[Pipe<DEC>::kStages][kSfaBytes];
+  uint8_t sfb[Pipe<DEC>::kStages][kSfbBytes];
+  uint64_t full[Pipe<DEC>::kStages];
+  uint64_t empty[Pipe<DEC>::kStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
   float amax_x[2][2][kBlockM];
@@ -74,33 +90,46 @@ struct __align__(1024) Smem {
   uint64_t sempty[kScaleSlots];
   uint32_t tmem_base;
   int abort_flag;
+  __device__ uint8_t* a_stage(int s) { return a + s * Pipe<DEC>::kAStride; }
 };
 
-static_assert(offsetof(Smem, sfa) % 16 == 0 && offsetof(Smem, sfb) % 16 == 0, "bulk copy alignment");
-static_assert(offsetof(Smem, sfa_w) % 16 == 0 && offsetof(Smem, sw) % 16 == 0, "bulk copy alignment");
-static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "shared memory budget");
+template <bool DEC>
+constexpr bool smem_layout_ok() {
+  return offsetof(SmemT<DEC>, a) % 1024 == 0 && Pipe<DEC>::kAStride % 1024 == 0 &&
+         offsetof(SmemT<DEC>, sfa) % 16 == 0 && offsetof(SmemT<DEC>, sfb) % 16 == 0 &&
+         offsetof(SmemT<DEC>, sfa_w) % 16 == 0 && offsetof(SmemT<DEC>, sw) % 16 == 0 &&
+         sizeof(SmemT<DEC>) + 1024 <= 227 * 1024 && kSfTmemCol + Pipe<DEC>::kStages * 12 <= kTmemCols;
+}
+static_assert(smem_layout_ok<false>() && smem_layout_ok<true>(), "shared / tensor memory layout");
 
 struct TileCoord {
   int e, mt, nt, row0, valid;
 };
 
-// idx -> (expert, m tile, n tile). Tiles are ordered expert-major, then by n
-// tile, with the expert's m tiles fastest, so CTAs running at the same time
-// share weight tiles through L2. Expert e owns idx in
-// [NT * mt_off[e], NT * mt_off[e + 1]), so idx / NT is one of e's global
-// m-tiles and the routing kernel's expert_of table gives e in one load.
-__device__ __forceinline__ TileCoord decode_tile(int idx, int E, int NT, const int32_t* __restrict__ mt_off,
+// Work unit idx -> (expert, token unit, n tile). A token unit is a 128-row
+// m-tile (tile mode) or a 32-row chunk (decode mode) of the expert's group.
+// Units are ordered expert-major, then by n tile, with the expert's token
+// units fastest, so CTAs running at the same time share weight tiles
+// through L2. Expert e owns idx in [NT * off[e], NT * off[e + 1]), so
+// idx / NT is one of e's token units and the routing kernel's owner table
+// gives e in one load.
+template <bool DEC>
+__device__ __forceinline__ TileCoord decode_tile(int idx, int E, int M, int NT, const int32_t* __restrict__ tiles,
                                                  const int32_t* __restrict__ counts,
                                                  const int32_t* __restrict__ padded_offsets) {
-  const int lo = __ldg(mt_off + (E + 1) + idx / NT);  // expert_of follows the E + 1 offsets
+  constexpr int kRows = Pipe<DEC>::kRows;
+  const int32_t* off = tiles + (DEC ? tiles_chunk_off(E) : kTilesHdr);
+  const int32_t* owner = tiles + (DEC ? tiles_chunk_expert(E, M) : tiles_expert_of(E));
+  const int e = __ldg(owner + idx / NT);
+  const int u0 = __ldg(off + e);
+  const int m_e = __ldg(off + e + 1) - u0;
+  const int local = idx - NT * u0;
   TileCoord c;
-  c.e = lo;
-  const int m_e = __ldg(mt_off + lo + 1) - __ldg(mt_off + lo);
-  const int local = idx - NT * __ldg(mt_off + lo);
+  c.e = e;
   c.nt = local / m_e;
   c.mt = local % m_e;
-  c.row0 = __ldg(padded_offsets + lo) + kBlockM * c.mt;
-  c.valid = min(kBlockM, __ldg(counts + lo) - kBlockM * c.mt);
+  c.row0 = __ldg(padded_offsets + e) + kRows * c.mt;
+  c.valid = min(kRows, __ldg(counts + e) - kRows * c.mt);
   return c;
 }
 
@@ -135,10 +164,13 @@ __device__ __forceinline__ float ue8m0_to_float(uint32_t b) {
 // promotion can use packed fp32x2 FMAs without re-pairing registers.
 #define ACC(i) (((i) & 1) ? acc2[(i) >> 1].y : acc2[(i) >> 1].x)
 
-template <int FMT, bool GEMM1>
+template <int FMT, bool GEMM1, bool DEC>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const GemmArgs args) {
+  static_assert(!DEC || FMT == MOE_W_FP4, "decode mode is built for FP4 weights");
+  using Smem = SmemT<DEC>;
+  constexpr int kStages = Pipe<DEC>::kStages;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned (SWIZZLE_128B atoms). The offset is applied to the
   // __shared__ array itself so the compiler keeps shared-space addressing.
@@ -146,8 +178,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const GemmGeom g = args.g;
   const int KB = g.KB, NT = g.NT;
-  const int32_t* mt_off = args.tiles + kTilesHdr;
   volatile int* abort_flag = &sm.abort_flag;
+  auto tile_of = [&](int idx) {
+    return decode_tile<DEC>(idx, args.E, args.M, NT, args.tiles, args.counts, args.padded_offsets);
+  };
 
   if (tid == 0) {
     sm.abort_flag = 0;
@@ -177,7 +211,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
   // the operands are written by the kernels before this one.
   pdl_wait();
   pdl_launch_dependents();
-  const int total_tiles = __ldg(args.tiles) * NT;
+  const int total_tiles = __ldg(args.tiles + (DEC ? 1 : 0)) * NT;
 
   if (warp < kEpiWarp0) {
    regs_dec<56>();
@@ -188,17 +222,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
       tma_prefetch_desc(&tmap_b);
       // The FP4 tile lands unpacked (16 codes per 16 bytes) but the copy's
       // transaction count is the packed global size.
-      const uint32_t bytes = (FMT == MOE_W_FP4) ? kTileABytes + kTileBBytes / 2 + kSfaBytes + kSfbBytes
-                                                : kTileABytes + kTileBBytes;
+      constexpr uint32_t kA = Pipe<DEC>::kAStride;
+      const uint32_t bytes = (FMT == MOE_W_FP4) ? kA + kTileBBytes / 2 + kSfaBytes + kSfbBytes : kA + kTileBBytes;
       int stage = 0;
       uint32_t phase = 0;
       for (int idx = blockIdx.x; idx < total_tiles && !*abort_flag; idx += gridDim.x) {
-        const TileCoord c = decode_tile(idx, args.E, NT, mt_off, args.counts, args.padded_offsets);
+        const TileCoord c = tile_of(idx);
         const int wrow = c.e * g.Np + c.nt * kBlockN;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(&sm.empty[stage], phase ^ 1, abort_flag)) break;
           mbar_arrive_expect_tx(&sm.full[stage], bytes);
-          tma_load_2d(sm.a[stage], &tmap_a, &sm.full[stage], kb * kBlockK, c.row0);
+          tma_load_2d(sm.a_stage(stage), &tmap_a, &sm.full[stage], kb * kBlockK, c.row0);
           tma_load_2d(sm.b[stage], &tmap_b, &sm.full[stage], kb * kBlockK, wrow);
           if constexpr (FMT == MOE_W_FP4) {
             bulk_load(sm.sfa[stage], args.a_sf + (static_cast<size_t>(c.row0 / kBlockM) * KB + kb) * kSfaBytes,
@@ -213,7 +247,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // One thread issues; in decode mode the whole warp walks the stages (it
+    // moves the chunk's activation scale words before each copy).
+    if (DEC || lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int buf = 0;
@@ -225,7 +261,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
             if (!mbar_wait_spin(&sm.full[stage], phase, abort_flag)) break;
             if (!mbar_wait_spin(&sm.tempty[buf], bphase ^ 1, abort_flag)) break;
             tc_fence_after();
-            const uint64_t ad = smem_desc(smem_u32(sm.a[stage]), 16, 1024, kSwizzle128B);
+            const uint64_t ad = smem_desc(smem_u32(sm.a_stage(stage)), 16, 1024, kSwizzle128B);
             const uint64_t bd = smem_desc(smem_u32(sm.b[stage]), 16, 1024, kSwizzle128B);
 #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -237,27 +273,50 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
             if (buf == 0) bphase ^= 1;
           }
         } else {
-          if (!mbar_wait(&sm.tempty[0], bphase ^ 1, abort_flag)) break;
+          bool ok = mbar_wait(&sm.tempty[0], bphase ^ 1, abort_flag);
+          if constexpr (DEC) ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
           tc_fence_after();
+          // Decode mode: the chunk's activation scale words are column q of
+          // its 128-row block's image; the MMA reads A rows 0-31 (the chunk)
+          // from the first column.
+          int q = 0;
+          if constexpr (DEC) q = (tile_of(idx).row0 % kBlockM) / kChunkRows;
           for (int kb = 0; kb < KB; ++kb) {
-            if (!mbar_wait(&sm.full[stage], phase, abort_flag)) break;
-            tc_fence_after();
-            const uint32_t sfa_col = kSfTmemCol + stage * 12;
-            const uint32_t sfb_col = sfa_col + 4;
-            tmem_cp_32x128b_warpx4(tbase + sfa_col, smem_desc(smem_u32(sm.sfa[stage]), 0, 128, kSwizzleNone));
-            tmem_cp_32x128b_warpx4(tbase + sfb_col, smem_desc(smem_u32(sm.sfb[stage]), 0, 128, kSwizzleNone));
-            tmem_cp_32x128b_warpx4(tbase + sfb_col + 4,
-                                   smem_desc(smem_u32(sm.sfb[stage] + 512), 0, 128, kSwizzleNone));
-            const uint64_t ad = smem_desc(smem_u32(sm.a[stage]), 16, 1024, kSwizzle128B);
-            const uint64_t bd = smem_desc(smem_u32(sm.b[stage]), 16, 1024, kSwizzle128B);
+            bool okf = mbar_wait(&sm.full[stage], phase, abort_flag);
+            if constexpr (DEC) okf = __all_sync(0xffffffffu, okf);
+            if (!okf) { ok = false; break; }
+            if constexpr (DEC) {
+              if (q != 0) {
+                uint32_t* w = reinterpret_cast<uint32_t*>(sm.sfa[stage]);
+                const uint32_t v = w[4 * lane + q];
+                __syncwarp();
+                w[4 * lane] = v;
+                fence_proxy_async_smem();
+                __syncwarp();
+              }
+            }
+            if (lane == 0) {
+              tc_fence_after();
+              const uint32_t sfa_col = kSfTmemCol + stage * 12;
+              const uint32_t sfb_col = sfa_col + 4;
+              tmem_cp_32x128b_warpx4(tbase + sfa_col, smem_desc(smem_u32(sm.sfa[stage]), 0, 128, kSwizzleNone));
+              tmem_cp_32x128b_warpx4(tbase + sfb_col, smem_desc(smem_u32(sm.sfb[stage]), 0, 128, kSwizzleNone));
+              tmem_cp_32x128b_warpx4(tbase + sfb_col + 4,
+                                     smem_desc(smem_u32(sm.sfb[stage] + 512), 0, 128, kSwizzleNone));
+              const uint64_t ad = smem_desc(smem_u32(sm.a_stage(stage)), 16, 1024, kSwizzle128B);
+              const uint64_t bd = smem_desc(smem_u32(sm.b[stage]), 16, 1024, kSwizzle128B);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              mma_mxf8f6f4(tbase, ad + 2 * j, bd + 2 * j, idesc_mxf8f6f4(0, 5, kBlockM, kBlockN, j, j),
-                           tbase + sfa_col, tbase + sfb_col, (kb > 0 || j > 0) ? 1u : 0u);
-            mma_commit(&sm.empty[stage]);
+              for (int j = 0; j < 4; ++j)
+                mma_mxf8f6f4(tbase, ad + 2 * j, bd + 2 * j, idesc_mxf8f6f4(0, 5, kBlockM, kBlockN, j, j),
+                             tbase + sfa_col, tbase + sfb_col, (kb > 0 || j > 0) ? 1u : 0u);
+              mma_commit(&sm.empty[stage]);
+            }
+            if constexpr (DEC) __syncwarp();
             if (++stage == kStages) { stage = 0; phase ^= 1; }
           }
-          mma_commit(&sm.tfull[0]);
+          if (!ok) break;
+          if (lane == 0) mma_commit(&sm.tfull[0]);
           bphase ^= 1;
         }
       }
@@ -271,7 +330,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
       int slot = 0;
       uint32_t sphase = 0;
       for (int idx = blockIdx.x; idx < total_tiles && !*abort_flag; idx += gridDim.x) {
-        const TileCoord c = decode_tile(idx, args.E, NT, mt_off, args.counts, args.padded_offsets);
+        const TileCoord c = tile_of(idx);
         for (int kb0 = 0; kb0 < KB; kb0 += kScaleGroup) {
           const int n = min(kScaleGroup, KB - kb0);
           if (!mbar_wait(&sm.sempty[slot], sphase ^ 1, abort_flag)) break;
@@ -300,7 +359,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
     const float limit = args.swiglu_limit;
     const bool clamp = limit > 0.f && limit < INFINITY;
     for (int idx = blockIdx.x; idx < total_tiles && !*abort_flag; idx += gridDim.x) {
-      const TileCoord c = decode_tile(idx, args.E, NT, mt_off, args.counts, args.padded_offsets);
+      const TileCoord c = tile_of(idx);
       float2 acc2[64];
       bool ok = true;
       if constexpr (FMT == MOE_W_FP8) {
@@ -440,11 +499,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
   if (tid == 0 && sm.abort_flag) atomicOr(args.status, MOE_DEV_TIMEOUT);
 }
 
-template <int FMT, bool GEMM1>
+template <int FMT, bool GEMM1, bool DEC>
 cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args, int num_sms,
                        cudaStream_t st) {
-  auto kern = grouped_gemm_kernel<FMT, GEMM1>;
-  const int smem = static_cast<int>(sizeof(Smem)) + 1024;
+  auto kern = grouped_gemm_kernel<FMT, GEMM1, DEC>;
+  const int smem = static_cast<int>(sizeof(SmemT<DEC>)) + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   return launch_kernel(true, kern, num_sms, kThreads, smem, st, ta, tb, args);
@@ -452,13 +511,16 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const GemmA
 
 }  // namespace
 
-cudaError_t launch_gemm(int fmt, bool is_gemm1, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args,
-                        int num_sms, cudaStream_t st) {
+cudaError_t launch_gemm(int fmt, bool is_gemm1, bool decode, const CUtensorMap& ta, const CUtensorMap& tb,
+                        const GemmArgs& args, int num_sms, cudaStream_t st) {
   if (fmt == MOE_W_FP8)
-    return is_gemm1 ? launch_one<MOE_W_FP8, true>(ta, tb, args, num_sms, st)
-                    : launch_one<MOE_W_FP8, false>(ta, tb, args, num_sms, st);
-  return is_gemm1 ? launch_one<MOE_W_FP4, true>(ta, tb, args, num_sms, st)
-                  : launch_one<MOE_W_FP4, false>(ta, tb, args, num_sms, st);
+    return is_gemm1 ? launch_one<MOE_W_FP8, true, false>(ta, tb, args, num_sms, st)
+                    : launch_one<MOE_W_FP8, false, false>(ta, tb, args, num_sms, st);
+  if (decode)
+    return is_gemm1 ? launch_one<MOE_W_FP4, true, true>(ta, tb, args, num_sms, st)
+                    : launch_one<MOE_W_FP4, false, true>(ta, tb, args, num_sms, st);
+  return is_gemm1 ? launch_one<MOE_W_FP4, true, false>(ta, tb, args, num_sms, st)
+                  : launch_one<MOE_W_FP4, false, false>(ta, tb, args, num_sms, st);
 }
 
 }  // namespace bsmoe

@@ -51,11 +51,18 @@ struct WsLayout {
 int route_chunks(int S);
 bool ws_layout(int fmt, int T, int H, int I, int E, int K, WsLayout* out);
 
-// Offsets inside the int32 "tiles" region: [0] = number of m-tiles;
-// [kTilesHdr + e] = m-tile offset of expert e (E + 1 entries);
-// [tiles_expert_of(E) + g] = expert owning global m-tile g (one per m-tile).
+// The int32 "tiles" region (GEMM work lists; M = padded row capacity):
+//   [0] number of 128-row m-tiles, [1] number of 32-row chunks;
+//   [kTilesHdr + e]                 first m-tile of expert e (E + 1 entries);
+//   [tiles_chunk_off(E) + e]        first chunk of expert e (E + 1 entries);
+//   [tiles_expert_of(E) + g]        expert owning m-tile g (M / 128 entries);
+//   [tiles_chunk_expert(E, M) + c]  expert owning chunk c (M / 32 entries).
 constexpr int kTilesHdr = 16;
-__host__ __device__ constexpr int tiles_expert_of(int E) { return kTilesHdr + E + 1; }
+constexpr int kChunkRows = 32;  // token rows per work unit of the decode-mode GEMMs
+__host__ __device__ constexpr int tiles_chunk_off(int E) { return kTilesHdr + E + 1; }
+__host__ __device__ constexpr int tiles_expert_of(int E) { return kTilesHdr + 2 * (E + 1); }
+__host__ __device__ constexpr int tiles_chunk_expert(int E, int M) { return tiles_expert_of(E) + M / kBlockM; }
+__host__ __device__ constexpr int tiles_ints(int E, int M) { return tiles_chunk_expert(E, M) + M / kChunkRows; }
 
 // Launches `kern` on `st`. With `dependent`, the launch may begin while the
 // preceding kernel in the stream is still running (programmatic stream
@@ -106,6 +113,7 @@ struct GemmArgs {
   int out_cols;               // GEMM1: act_cols (= Kp of GEMM2); GEMM2: H
   int out_blocks;             // GEMM1: act_blocks
   int E, I, H;
+  int M;                      // padded row capacity (locates the chunk work list)
   float swiglu_limit;         // > 0 and finite: clamp
   GemmGeom g;
 };
@@ -116,7 +124,11 @@ moe_status forward_impl(const void* hidden, const int32_t* topk_idx, const float
                         int E, int K, int fmt, const void* w13_prep, const void* w2_prep, float swiglu_limit,
                         void* workspace, size_t workspace_bytes, void* out, void* stream, void* const* events);
 
-cudaError_t launch_gemm(int fmt, bool is_gemm1, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+// decode: FP4 only; 32-row token chunks, activation tensor maps with a
+// 32-row box (tile mode: 128-row m-tiles, 128-row box). Chosen when the
+// pairs per expert average at most kDecodePairsPerExpert.
+constexpr int kDecodePairsPerExpert = 8;
+cudaError_t launch_gemm(int fmt, bool is_gemm1, bool decode, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                         const GemmArgs& args, int num_sms, cudaStream_t st);
 
 }  // namespace bsmoe

@@ -115,7 +115,7 @@ __device__ __forceinline__ int warp_incl_scan(int x) {
 
 __global__ void __launch_bounds__(kQuantWarps * 32)
 route_quant_small_kernel(const int32_t* __restrict__ idx, const __nv_bfloat16* __restrict__ hidden, int S, int E,
-                         int K, int H, int Kp, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                         int K, int H, int Kp, int M, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                          int32_t* __restrict__ padded_offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
                          int32_t* __restrict__ row_slot, int32_t* __restrict__ tiles, uint32_t* __restrict__ status,
                          uint8_t* __restrict__ xq, uint32_t* __restrict__ xsf) {
@@ -126,7 +126,8 @@ route_quant_small_kernel(const int32_t* __restrict__ idx, const __nv_bfloat16* _
   __shared__ int off[kMaxExperts + 1];
   __shared__ int pad[kMaxExperts + 1];
   __shared__ int mts[kMaxExperts + 1];
-  __shared__ int wsum[3][kQuantWarps];
+  __shared__ int chs[kMaxExperts + 1];
+  __shared__ int wsum[4][kQuantWarps];
   __shared__ int rows[kMaxTopK];
   __shared__ int nrows;
   __shared__ int bad;
@@ -146,27 +147,31 @@ route_quant_small_kernel(const int32_t* __restrict__ idx, const __nv_bfloat16* _
   __syncthreads();
 
   // Exclusive scans over the E + 1 keys of: counts, counts padded to the
-  // group alignment, m-tiles. Thread i owns entries [kScanPer i, kScanPer i + kScanPer).
+  // group alignment, 128-row m-tiles, 32-row chunks. Thread i owns entries
+  // [kScanPer i, kScanPer i + kScanPer).
   {
-    int c[kScanPer], a[3] = {0, 0, 0};
+    int v[kScanPer][4], a[4] = {0, 0, 0, 0};
 #pragma unroll
     for (int j = 0; j < kScanPer; ++j) {
       const int e = tid * kScanPer + j;
-      c[j] = (e < E) ? cnt[e] : 0;  // the skipped key E takes no rows
-      a[0] += c[j];
-      a[1] += (c[j] + kRowAlign - 1) / kRowAlign * kRowAlign;
-      a[2] += (c[j] + kBlockM - 1) / kBlockM;
-    }
-    int inc[3];
+      const int c = (e < E) ? cnt[e] : 0;  // the skipped key E takes no rows
+      v[j][0] = c;
+      v[j][1] = (c + kRowAlign - 1) / kRowAlign * kRowAlign;
+      v[j][2] = (c + kBlockM - 1) / kBlockM;
+      v[j][3] = (c + kChunkRows - 1) / kChunkRows;
 #pragma unroll
-    for (int q = 0; q < 3; ++q) {
+      for (int q = 0; q < 4; ++q) a[q] += v[j][q];
+    }
+    int inc[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
       inc[q] = warp_incl_scan(a[q]);
       if (lane == 31) wsum[q][warp] = inc[q];
     }
     __syncthreads();
-    int base[3];
+    int base[4];
 #pragma unroll
-    for (int q = 0; q < 3; ++q) {
+    for (int q = 0; q < 4; ++q) {
       int b = 0;
       for (int w = 0; w < warp; ++w) b += wsum[q][w];
       base[q] = b + inc[q] - a[q];
@@ -178,10 +183,10 @@ route_quant_small_kernel(const int32_t* __restrict__ idx, const __nv_bfloat16* _
         off[e] = base[0];
         pad[e] = base[1];
         mts[e] = base[2];
+        chs[e] = base[3];
       }
-      base[0] += c[j];
-      base[1] += (c[j] + kRowAlign - 1) / kRowAlign * kRowAlign;
-      base[2] += (c[j] + kBlockM - 1) / kBlockM;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) base[q] += v[j][q];
     }
   }
   // Stable rank of every slot among the slots with the same key.
@@ -201,13 +206,16 @@ route_quant_small_kernel(const int32_t* __restrict__ idx, const __nv_bfloat16* _
       offsets[E] = off[E];
       padded_offsets[E] = pad[E];
       tiles[0] = mts[E];
+      tiles[1] = chs[E];
       tiles[kTilesHdr + E] = mts[E];
+      tiles[tiles_chunk_off(E) + E] = chs[E];
     }
     for (int e = tid; e < E; e += kThreads) {
       counts[e] = cnt[e];
       offsets[e] = off[e];
       padded_offsets[e] = pad[e];
       tiles[kTilesHdr + e] = mts[e];
+      tiles[tiles_chunk_off(E) + e] = chs[e];
     }
     for (int s = tid; s < S; s += kThreads) {
       const int k = key[s];
@@ -221,8 +229,10 @@ route_quant_small_kernel(const int32_t* __restrict__ idx, const __nv_bfloat16* _
       }
     }
     int32_t* expert_of = tiles + tiles_expert_of(E);
+    int32_t* chunk_expert = tiles + tiles_chunk_expert(E, M);
     for (int e = warp; e < E; e += kQuantWarps) {
       for (int g = mts[e] + lane; g < mts[e + 1]; g += 32) expert_of[g] = e;
+      for (int g = chs[e] + lane; g < chs[e + 1]; g += 32) chunk_expert[g] = e;
       for (int r = pad[e] + cnt[e] + lane; r < pad[e + 1]; r += 32) row_slot[r] = -1;  // padding rows
     }
   }
@@ -255,7 +265,7 @@ cudaError_t launch_route_quant_small(const int32_t* topk_idx, const void* hidden
   // The first kernel of the forward is an ordinary launch: it follows
   // whatever the caller queued on the stream.
   return launch_kernel(false, route_quant_small_kernel, T, kQuantWarps * 32, 0, st, topk_idx,
-                       reinterpret_cast<const __nv_bfloat16*>(hidden), T * K, E, K, H, p.xq_cols,
+                       reinterpret_cast<const __nv_bfloat16*>(hidden), T * K, E, K, H, p.xq_cols, L.M,
                        reinterpret_cast<int32_t*>(ws + p.counts), reinterpret_cast<int32_t*>(ws + p.offsets),
                        reinterpret_cast<int32_t*>(ws + p.padded_offsets), reinterpret_cast<int32_t*>(ws + p.perm),
                        reinterpret_cast<int32_t*>(ws + p.inv), reinterpret_cast<int32_t*>(ws + p.row_slot),

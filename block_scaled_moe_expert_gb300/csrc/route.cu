@@ -67,6 +67,48 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_sums, int* total
   return r;
 }
 
+// From the slot count c_e of expert tid (tid < E, 0 otherwise; 1024
+// threads): the exclusive scans of the counts, of the counts padded to the
+// group alignment, of the 128-row m-tiles and of the 32-row chunks; writes
+// counts, offsets, padded_offsets and the GEMM work lists of the tiles
+// region, and leaves the offsets and group starts in s_off / s_pad.
+__device__ void scan_counts_and_tables(int E, int M, int c_e, int32_t* __restrict__ counts,
+                                       int32_t* __restrict__ offsets, int32_t* __restrict__ padded_offsets,
+                                       int32_t* __restrict__ tiles, int* s_off, int* s_pad, int* s_mt, int* s_ch,
+                                       int* warp_sums, int* tot) {
+  const int tid = threadIdx.x;
+  const int off = block_excl_scan(c_e, warp_sums, &tot[0]);
+  const int pad = block_excl_scan((c_e + kRowAlign - 1) / kRowAlign * kRowAlign, warp_sums, &tot[1]);
+  const int mts = block_excl_scan((c_e + kBlockM - 1) / kBlockM, warp_sums, &tot[2]);
+  const int chs = block_excl_scan((c_e + kChunkRows - 1) / kChunkRows, warp_sums, &tot[3]);
+  if (tid < E) {
+    counts[tid] = c_e;
+    offsets[tid] = off;
+    padded_offsets[tid] = pad;
+    tiles[kTilesHdr + tid] = mts;
+    tiles[tiles_chunk_off(E) + tid] = chs;
+    s_off[tid] = off;
+    s_pad[tid] = pad;
+    s_mt[tid] = mts;
+    s_ch[tid] = chs;
+  }
+  if (tid == 0) {
+    offsets[E] = tot[0];
+    padded_offsets[E] = tot[1];
+    tiles[0] = tot[2];
+    tiles[1] = tot[3];
+    tiles[kTilesHdr + E] = tot[2];
+    tiles[tiles_chunk_off(E) + E] = tot[3];
+    s_off[E] = tot[0];
+    s_pad[E] = tot[1];
+    s_mt[E] = tot[2];
+    s_ch[E] = tot[3];
+  }
+  __syncthreads();
+  write_expert_of(E, s_mt, tiles + tiles_expert_of(E));
+  write_expert_of(E, s_ch, tiles + tiles_chunk_expert(E, M));
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 route_kernel(const int32_t* __restrict__ idx, int S, int E, int M, int32_t* __restrict__ counts,
              int32_t* __restrict__ offsets, int32_t* __restrict__ padded_offsets, int32_t* __restrict__ perm,
@@ -74,10 +116,11 @@ route_kernel(const int32_t* __restrict__ idx, int S, int E, int M, int32_t* __re
              uint32_t* __restrict__ status) {
   extern __shared__ int hist[];  // [kWarps][E + 1]
   __shared__ int warp_sums[32];
-  __shared__ int tot[3];
+  __shared__ int tot[4];
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_pad[kMaxExperts + 1];
   __shared__ int s_mt[kMaxExperts + 1];
+  __shared__ int s_ch[kMaxExperts + 1];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int stride = E + 1;
   pdl_wait();
@@ -117,29 +160,7 @@ route_kernel(const int32_t* __restrict__ idx, int S, int E, int M, int32_t* __re
     cnt = run;
   }
   const int c_e = (tid < E) ? cnt : 0;
-  const int off = block_excl_scan(c_e, warp_sums, &tot[0]);
-  const int pad = block_excl_scan((c_e + kRowAlign - 1) / kRowAlign * kRowAlign, warp_sums, &tot[1]);
-  const int mts = block_excl_scan((c_e + kBlockM - 1) / kBlockM, warp_sums, &tot[2]);
-  if (tid < E) {
-    counts[tid] = c_e;
-    offsets[tid] = off;
-    padded_offsets[tid] = pad;
-    tiles[kTilesHdr + tid] = mts;
-    s_off[tid] = off;
-    s_pad[tid] = pad;
-    s_mt[tid] = mts;
-  }
-  if (tid == 0) {
-    offsets[E] = tot[0];
-    padded_offsets[E] = tot[1];
-    tiles[kTilesHdr + E] = tot[2];
-    tiles[0] = tot[2];
-    s_off[E] = tot[0];
-    s_pad[E] = tot[1];
-    s_mt[E] = tot[2];
-  }
-  __syncthreads();
-  write_expert_of(E, s_mt, tiles + tiles_expert_of(E));
+  scan_counts_and_tables(E, M, c_e, counts, offsets, padded_offsets, tiles, s_off, s_pad, s_mt, s_ch, warp_sums, tot);
 
   // Pass 2: scatter.
   for (int base = beg; base < end; base += 32) {
@@ -171,7 +192,6 @@ route_kernel(const int32_t* __restrict__ idx, int S, int E, int M, int32_t* __re
     const int hi = s_pad[e + 1];
     for (int r = lo + lane; r < hi; r += 32) row_slot[r] = -1;
   }
-  (void)M;
 }
 
 // ---------------------------------------------------------------------------
@@ -199,14 +219,15 @@ route_hist_kernel(const int32_t* __restrict__ idx, int S, int E, int32_t* __rest
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-route_scan_kernel(int E, int G, int32_t* __restrict__ chunk_hist, int32_t* __restrict__ counts,
+route_scan_kernel(int E, int M, int G, int32_t* __restrict__ chunk_hist, int32_t* __restrict__ counts,
                   int32_t* __restrict__ offsets, int32_t* __restrict__ padded_offsets,
                   int32_t* __restrict__ row_slot, int32_t* __restrict__ tiles, uint32_t* __restrict__ status) {
   __shared__ int warp_sums[32];
-  __shared__ int tot[3];
+  __shared__ int tot[4];
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_pad[kMaxExperts + 1];
   __shared__ int s_mt[kMaxExperts + 1];
+  __shared__ int s_ch[kMaxExperts + 1];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_wait();
   pdl_launch_dependents();
@@ -225,29 +246,7 @@ route_scan_kernel(int E, int G, int32_t* __restrict__ chunk_hist, int32_t* __res
     cnt = run;
   }
   const int c_e = (tid < E) ? cnt : 0;
-  const int off = block_excl_scan(c_e, warp_sums, &tot[0]);
-  const int pad = block_excl_scan((c_e + kRowAlign - 1) / kRowAlign * kRowAlign, warp_sums, &tot[1]);
-  const int mts = block_excl_scan((c_e + kBlockM - 1) / kBlockM, warp_sums, &tot[2]);
-  if (tid < E) {
-    counts[tid] = c_e;
-    offsets[tid] = off;
-    padded_offsets[tid] = pad;
-    tiles[kTilesHdr + tid] = mts;
-    s_off[tid] = off;
-    s_pad[tid] = pad;
-    s_mt[tid] = mts;
-  }
-  if (tid == 0) {
-    offsets[E] = tot[0];
-    padded_offsets[E] = tot[1];
-    tiles[kTilesHdr + E] = tot[2];
-    tiles[0] = tot[2];
-    s_off[E] = tot[0];
-    s_pad[E] = tot[1];
-    s_mt[E] = tot[2];
-  }
-  __syncthreads();
-  write_expert_of(E, s_mt, tiles + tiles_expert_of(E));
+  scan_counts_and_tables(E, M, c_e, counts, offsets, padded_offsets, tiles, s_off, s_pad, s_mt, s_ch, warp_sums, tot);
   for (int e = warp; e < E; e += kWarps) {
     const int lo = s_pad[e] + (s_off[e + 1] - s_off[e]);
     const int hi = s_pad[e + 1];
@@ -336,7 +335,7 @@ cudaError_t launch_route(const int32_t* topk_idx, int S, int E, const WsLayout& 
     cudaError_t e = launch_kernel(false, route_hist_kernel, G, kChunkWarps * 32, sizeof(int) * (E + 1), st,
                                   topk_idx, S, E, chunk_hist);
     if (e != cudaSuccess) return e;
-    e = launch_kernel(true, route_scan_kernel, 1, kThreads, 0, st, E, G, chunk_hist,
+    e = launch_kernel(true, route_scan_kernel, 1, kThreads, 0, st, E, L.M, G, chunk_hist,
                       reinterpret_cast<int32_t*>(ws + p.counts), reinterpret_cast<int32_t*>(ws + p.offsets),
                       reinterpret_cast<int32_t*>(ws + p.padded_offsets), reinterpret_cast<int32_t*>(ws + p.row_slot),
                       reinterpret_cast<int32_t*>(ws + p.tiles), status);

@@ -230,6 +230,10 @@ moe_status moe_get_device_status(void* workspace, void* stream, uint32_t* flags)
  *   perm [S] (sorted position -> slot, skipped slots last);
  *   inv [S] (slot -> padded row, -1 if skipped);
  *   row_slot [M] (padded row -> slot, -1 for padding rows);
+ *   tiles [16 + 2 (E+1) + M/128 + M/32] (GEMM work lists): [0] number of
+ *     128-row m-tiles, [1] number of 32-row chunks, [16 + e] first m-tile
+ *     and [16 + E + 1 + e] first chunk of expert e (E+1 entries each), then
+ *     the expert owning each m-tile, then the expert owning each chunk;
  *   tiles [16 + (E+1) + M/128]: [0] number of 128-row m-tiles, [16 + e]
  *     first m-tile of expert e (E+1 entries), then the expert owning each
  *     m-tile (GEMM work list);

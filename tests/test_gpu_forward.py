@@ -26,6 +26,11 @@ CASES = [
     W.Workload("fp4_small_ragged", 40, 320, 192, 8, 3, "fp4", "softmax", seed=17, swiglu_limit=0.25),
     W.Workload("fp4_small_zipf", 64, 512, 256, 32, 8, "fp4", "zipf_sigmoid", seed=18, skip_frac=0.05),
     W.Workload("fp4_small_T1", 1, 512, 384, 16, 4, "fp4", "softmax", seed=19),
+    # FP4 with at most 8 pairs per expert on average: the decode mode of the
+    # grouped GEMMs (32-row token chunks). Zipf routing gives some experts
+    # 2-4 chunks, i.e. chunks in every 32-row quarter of a 128-row block.
+    W.Workload("fp4_decode_chunks", 40, 320, 192, 64, 8, "fp4", "zipf_sigmoid", seed=24, swiglu_limit=0.25),
+    W.Workload("fp4_decode_dsv3_like", 48, 1024, 512, 64, 8, "fp4", "zipf_sigmoid", seed=25, skip_frac=0.05),
 ]
 
 
@@ -148,3 +153,16 @@ def test_fp4_token_outputs_do_not_depend_on_the_batch():
     w = torch.cat([r["w"], torch.rand(extra, wl.K, generator=g, device="cuda")])
     out = P.B.experts_forward(hid, idx, w, r["prepared"])
     assert torch.equal(out[:wl.T].view(torch.int16), r["out"].view(torch.int16))
+
+
+def test_fp4_decode_mode_expert_with_four_chunks():
+    """One expert takes 100 tokens in a batch with at most 8 pairs per expert
+    on average: its rows span four 32-row chunks, one in each quarter of its
+    128-row block (each chunk's scale words sit in a different column)."""
+    wl = W.Workload("fp4_four_chunks", 100, 512, 256, 64, 2, "fp4", "softmax", seed=26, swiglu_limit=3.0)
+    idx, w = W.make_routing(wl, "cuda")
+    idx[:, 0] = 5
+    idx[:, 1] = torch.where(idx[:, 1] == 5, torch.full_like(idx[:, 1], 6), idx[:, 1])
+    r = P.run_cuda(wl, idx=idx, w=w)
+    ref = P.oracle_out(r["hidden"], r["idx"], r["w"], r["weights"], wl.swiglu_limit)
+    P.assert_close(r["out"], ref, "four chunks")

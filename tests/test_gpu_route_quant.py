@@ -28,14 +28,21 @@ def _check_route_quant(wl, r):
     assert (inv == ref["inv"]).all()
     M = int(ref["padded_offsets"][E])
     assert (get("row_slot", M) == ref["row_slot"]).all()
-    # GEMM work list: m-tile offsets per expert and the expert of each m-tile
+    # GEMM work lists: 128-row m-tiles and 32-row chunks per expert, their
+    # offsets and the expert owning each
     mtiles = -(-ref["counts"] // 128)
+    chunks = -(-ref["counts"] // 32)
     mt_off = np.concatenate([[0], np.cumsum(mtiles)])
-    n_mt = int(mt_off[-1])
-    tiles = get("tiles", 16 + E + 1 + n_mt)
-    assert tiles[0] == n_mt
+    ch_off = np.concatenate([[0], np.cumsum(chunks)])
+    n_mt, n_ch = int(mt_off[-1]), int(ch_off[-1])
+    Mcap = L.row_capacity
+    base = 16 + 2 * (E + 1)
+    tiles = get("tiles", base + Mcap // 128 + n_ch)
+    assert tiles[0] == n_mt and tiles[1] == n_ch
     assert (tiles[16:16 + E + 1] == mt_off).all()
-    assert (tiles[16 + E + 1:] == np.repeat(np.arange(E), mtiles)).all()
+    assert (tiles[16 + E + 1:base] == ch_off).all()
+    assert (tiles[base:base + n_mt] == np.repeat(np.arange(E), mtiles)).all()
+    assert (tiles[base + Mcap // 128:] == np.repeat(np.arange(E), chunks)).all()
 
     codes, exps = P.OM.quantize_hidden(P.bits_of(r["hidden"]))
     valid = np.flatnonzero(ref["inv"] >= 0)
