@@ -29,41 +29,54 @@ constexpr int kQuantWarps = 8;
 // in `rows`. A warp covers 256 columns (two 128-column blocks) per step: each
 // lane loads 8 bf16 (16 bytes), the 16 lanes of a half-warp reduce the
 // block's amax, and each lane stores 8 code bytes per destination row, so a
-// warp writes 256 contiguous bytes of every row it copies to.
+// warp writes 256 contiguous bytes of every row it copies to. The loads of
+// kLoadBatch steps are issued together, so a row (up to 8 x 256 x kLoadBatch
+// columns) costs one memory latency instead of one per step.
+constexpr int kLoadBatch = 4;
 __device__ __forceinline__ void quantize_token(const __nv_bfloat16* __restrict__ xr, int H, int Kp,
                                                const int* rows, int n, uint8_t* __restrict__ xq,
                                                uint32_t* __restrict__ xsf) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nblk = Kp / 128;
-  for (int c0w = warp * 256; c0w < Kp; c0w += kQuantWarps * 256) {
-    const int c0 = c0w + lane * 8;
-    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (c0 < H) {  // H % 64 == 0: a lane's 8 columns are all in or all out
-      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(xr + c0));
-      const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+  constexpr int kStep = kQuantWarps * 256;
+  for (int base = warp * 256; base < Kp; base += kStep * kLoadBatch) {
+    uint4 raw[kLoadBatch];
+#pragma unroll
+    for (int u = 0; u < kLoadBatch; ++u) {
+      const int c0 = base + u * kStep + lane * 8;
+      // H % 64 == 0: a lane's 8 columns are all in or all out
+      raw[u] = (c0 < H) ? __ldg(reinterpret_cast<const uint4*>(xr + c0)) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kLoadBatch; ++u) {
+      const int c0w = base + u * kStep;
+      if (c0w >= Kp) break;
+      const int c0 = c0w + lane * 8;
+      float v[8];
+      const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw[u]);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         v[2 * i] = __low2float(p2[i]);
         v[2 * i + 1] = __high2float(p2[i]);
       }
-    }
-    float amax = 0.f;
+      float amax = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
 #pragma unroll
-    for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const int e = act_exponent(amax);
-    const float s = exp2_neg(e);
-    const uint2 q = make_uint2(pack4_e4m3(v[0] * s, v[1] * s, v[2] * s, v[3] * s),
-                               pack4_e4m3(v[4] * s, v[5] * s, v[6] * s, v[7] * s));
-    const uint32_t word = static_cast<uint32_t>(e + 127) * 0x01010101u;
-    const bool in_range = c0 < Kp;
-    const int blk = c0 / 128;
-    for (int i = 0; i < n; ++i) {
-      const int r = rows[i];
-      if (in_range) {
-        *reinterpret_cast<uint2*>(xq + static_cast<size_t>(r) * Kp + c0) = q;
-        if ((lane & 15) == 0) xsf[sf_word_index(r, blk, nblk)] = word;
+      for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const int e = act_exponent(amax);
+      const float s = exp2_neg(e);
+      const uint2 q = make_uint2(pack4_e4m3(v[0] * s, v[1] * s, v[2] * s, v[3] * s),
+                                 pack4_e4m3(v[4] * s, v[5] * s, v[6] * s, v[7] * s));
+      const uint32_t word = static_cast<uint32_t>(e + 127) * 0x01010101u;
+      const bool in_range = c0 < Kp;
+      const int blk = c0 / 128;
+      for (int i = 0; i < n; ++i) {
+        const int r = rows[i];
+        if (in_range) {
+          *reinterpret_cast<uint2*>(xq + static_cast<size_t>(r) * Kp + c0) = q;
+          if ((lane & 15) == 0) xsf[sf_word_index(r, blk, nblk)] = word;
+        }
       }
     }
   }
@@ -228,12 +241,16 @@ route_quant_small_kernel(const int32_t* __restrict__ idx, const __nv_bfloat16* _
         inv[s] = -1;
       }
     }
+    // Work lists and padding rows, one thread per expert (at most 256
+    // slots, so few experts have any).
     int32_t* expert_of = tiles + tiles_expert_of(E);
     int32_t* chunk_expert = tiles + tiles_chunk_expert(E, M);
-    for (int e = warp; e < E; e += kQuantWarps) {
-      for (int g = mts[e] + lane; g < mts[e + 1]; g += 32) expert_of[g] = e;
-      for (int g = chs[e] + lane; g < chs[e + 1]; g += 32) chunk_expert[g] = e;
-      for (int r = pad[e] + cnt[e] + lane; r < pad[e + 1]; r += 32) row_slot[r] = -1;  // padding rows
+    for (int e = tid; e < E; e += kThreads) {
+      const int c = cnt[e];
+      if (c == 0) continue;
+      for (int g = mts[e]; g < mts[e + 1]; ++g) expert_of[g] = e;
+      for (int g = chs[e]; g < chs[e + 1]; ++g) chunk_expert[g] = e;
+      for (int r = pad[e] + c; r < pad[e + 1]; ++r) row_slot[r] = -1;  // padding rows
     }
   }
 
