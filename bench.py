@@ -40,7 +40,7 @@ UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 STAGES = ["route", "quant", "gemm1", "gemm2", "combine"]
 L2_FLUSH_BYTES = 256 << 20
-CPU_SAMPLE_TOKENS = {"mixtral_prefill_fp8": 12, "dsv3_prefill_fp8": 3, "dsv3_decode_fp8": 3, "gptoss_fp8xfp4": 24}
+CPU_SAMPLE_TOKENS = {"mixtral_prefill_fp8": 24, "dsv3_prefill_fp8": 3, "dsv3_decode_fp8": 3, "gptoss_fp8xfp4": 24}
 
 
 def load_peaks():
