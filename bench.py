@@ -109,11 +109,13 @@ def weight_bytes_per_expert(wl, which):
 def launches_per_forward(wl):
     """Kernels one forward launches: routing + quantization (one fused kernel
     up to 256 slots; else one routing kernel up to 8192 slots or histogram +
-    scan + scatter, then the quantization kernel), GEMM1, GEMM2, combine."""
+    scan + scatter, then the quantization kernel), GEMM1, GEMM2, and the
+    combine (inside GEMM2 for FP4 weights with at most 8 pairs per expert
+    and at most 256 slots)."""
     S = wl.T * wl.K
-    if S <= 256:
-        return 4
-    return (1 if S <= 8192 else 3) + 4
+    front = 1 if S <= 256 else (2 if S <= 8192 else 4)
+    combine = 0 if (wl.fmt == "fp4" and S <= 8 * wl.E and S <= 256) else 1
+    return front + 2 + combine
 
 
 def routing_stats(idx_cpu, E):

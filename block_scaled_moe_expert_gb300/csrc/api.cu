@@ -131,6 +131,10 @@ bool ws_layout(int fmt, int T, int H, int I, int E, int K, WsLayout* out) {
   p.asf = take(4ull * M * g2.KB);
   p.y = take(4ull * M * H);
   L.route_scratch = take(4ull * (static_cast<size_t>(route_chunks(static_cast<int>(S))) + 1) * (E + 1));
+  if (fused_combine(fmt, S, E)) {
+    L.combine_stride = 1 + kCombineSplits * g2.NT;
+    L.combine_cnt = take(4ull * static_cast<size_t>(T) * L.combine_stride);
+  }
   p.total_bytes = off;
   p.row_capacity = static_cast<int32_t>(M);
   p.row_align = kRowAlign;
@@ -276,7 +280,7 @@ moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, cons
   const bool fp4 = (fmt == MOE_W_FP4);
   // FP4 weights with few pairs per expert: the weight-streaming decode mode
   // of the grouped GEMMs (32-row token chunks, five weight stages).
-  const bool decode = fp4 && static_cast<long long>(L.S) <= static_cast<long long>(kDecodePairsPerExpert) * E;
+  const bool decode = decode_mode(fmt, L.S, E);
   const int a_box = decode ? kChunkRows : kBlockM;
 
   CUtensorMap ta1, tb1, ta2, tb2;
@@ -295,7 +299,8 @@ moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, cons
   if (!mark(0)) return MOE_ERR_CUDA;
   if (L.S <= kFusedRouteQuantSlots) {
     // One launch for both (the quant stage then has zero length).
-    if (launch_route_quant_small(topk_idx, hidden, T, H, E, K, L, ws, st) != cudaSuccess || !mark(1) || !mark(2))
+    if (launch_route_quant_small(topk_idx, hidden, T, H, E, K, L, ws, out, st) != cudaSuccess || !mark(1) ||
+        !mark(2))
       return MOE_ERR_CUDA;
   } else {
     if (launch_route(topk_idx, L.S, E, L, ws, st) != cudaSuccess || !mark(1)) return MOE_ERR_CUDA;
@@ -330,13 +335,23 @@ moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, cons
   a2.a_sf = ws + p.asf;
   a2.w_scale = static_cast<const uint8_t*>(w2_prep) + P2.scale_off;
   a2.out_y = reinterpret_cast<float*>(ws + p.y);
+  const bool fuse_combine = fused_combine(fmt, L.S, E);
+  if (fuse_combine) {
+    a2.inv = reinterpret_cast<const int32_t*>(ws + p.inv);
+    a2.combine_cnt = reinterpret_cast<int32_t*>(ws + L.combine_cnt);
+    a2.combine_stride = L.combine_stride;
+    a2.K = K;
+    a2.out = static_cast<__nv_bfloat16*>(out);
+  }
   a2.out_cols = H;
   a2.g = g2;
   if (launch_gemm(fmt, false, decode, ta2, tb2, a2, d.sms, st) != cudaSuccess || !mark(4)) return MOE_ERR_CUDA;
 
-  if (launch_combine(reinterpret_cast<const float*>(ws + p.y), reinterpret_cast<const int32_t*>(ws + p.inv), T, H,
-                     K, out, st) != cudaSuccess || !mark(5))
+  // With the fused combine GEMM2 already wrote the output.
+  if (!fuse_combine && launch_combine(reinterpret_cast<const float*>(ws + p.y), reinterpret_cast<const int32_t*>(ws + p.inv),
+                                T, H, K, out, st) != cudaSuccess)
     return MOE_ERR_CUDA;
+  if (!mark(5)) return MOE_ERR_CUDA;
   return MOE_OK;
 }
 

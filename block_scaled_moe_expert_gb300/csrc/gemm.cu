@@ -472,6 +472,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
         }
       } else {
         if (!ok) break;
+        bool last = false;
+        int t_last = 0;
         if (m < c.valid) {
           const int slot = __ldg(args.row_slot + row);
           const float wgt = __ldg(args.topk_w + slot);
@@ -486,6 +488,69 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
               st_global_v8(dst + 8 * v, __float_as_uint(p0.x), __float_as_uint(p0.y), __float_as_uint(p1.x),
                            __float_as_uint(p1.y), __float_as_uint(p2.x), __float_as_uint(p2.y), __float_as_uint(p3.x),
                            __float_as_uint(p3.y));
+            }
+          }
+          if (DEC && args.combine_cnt != nullptr) {
+            // Fused combine: count this row's arrival for its token and these
+            // 128 columns (the combine itself runs warp-wide below).
+            t_last = slot / args.K;
+            __threadfence();  // this row is visible before it is counted
+            int32_t* cnt = args.combine_cnt + static_cast<size_t>(t_last) * args.combine_stride;
+            last = (atomicAdd(cnt + 1 + kCombineSplits * c.nt + wg, 1) + 1) == __ldg(cnt);
+          }
+        }
+        if (DEC && args.combine_cnt != nullptr) {
+          // Fused combine (decode mode, small batches): the top-k combine. The last of a token's rows to
+          // arrive for these 128 columns triggers the sum of all of them in
+          // ascending k, in fp32, rounded once to bf16 - the deterministic
+          // reduction of the pages (view(T, K, H).sum(1), no atomics on data),
+          // whatever the order in which the tiles finish. The warp serves its
+          // last arrivers one by one, each lane summing 4 of the 128 columns
+          // with all K row loads in flight together.
+          unsigned todo = __ballot_sync(0xffffffffu, last);
+          if (todo) {
+            // the counting thread's fence, then the warp barrier, order the
+            // other rows' stores before every lane's loads
+            __threadfence();
+            __syncwarp();
+          }
+          const int col0 = c.nt * kBlockN + wg * 128 + 4 * lane;
+          while (todo) {
+            const int src = __ffs(todo) - 1;
+            todo &= todo - 1;
+            const int t = __shfl_sync(0xffffffffu, t_last, src);
+            const int my_row = (lane < args.K) ? __ldg(args.inv + static_cast<size_t>(t) * args.K + lane) : -1;
+            // H may end halfway through these 128 columns: lanes past it load
+            // nothing, but every lane stays in the shuffles
+            const bool in_h = col0 < args.H;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int k0 = 0; k0 < args.K; k0 += 8) {
+              int r[8];
+              float4 v[8];
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                r[u] = __shfl_sync(0xffffffffu, my_row, (k0 + u) & 31);
+                if (k0 + u >= args.K) r[u] = -1;
+                v[u] = (in_h && r[u] >= 0)
+                           ? __ldcg(reinterpret_cast<const float4*>(args.out_y + static_cast<size_t>(r[u]) * args.H + col0))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                if (r[u] >= 0) {
+                  acc.x += v[u].x;
+                  acc.y += v[u].y;
+                  acc.z += v[u].z;
+                  acc.w += v[u].w;
+                }
+              }
+            }
+            if (in_h) {
+              const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+              uint2 pk;
+              pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+              pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+              *reinterpret_cast<uint2*>(args.out + static_cast<size_t>(t) * args.H + col0) = pk;
             }
           }
         }

@@ -3,6 +3,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "moe_experts.h"
@@ -41,10 +42,23 @@ PrepLayout prep_layout(int fmt, int E, const GemmGeom& g);
 GemmGeom geom_w13(int H, int I);
 GemmGeom geom_w2(int H, int I);
 
+// Decode mode (FP4 weights, at most kDecodePairsPerExpert pairs per expert
+// on average): 32-row token chunks in the GEMMs.
+constexpr int kDecodePairsPerExpert = 8;
+constexpr int kCombineSplits = 2;  // column halves of a GEMM2 tile row, finished by separate warpgroups
+inline bool decode_mode(int fmt, long long S, int E) {
+  return fmt == MOE_W_FP4 && S <= static_cast<long long>(kDecodePairsPerExpert) * E;
+}
+
 struct WsLayout {
   moe_workspace_layout pub;
   int S, M, max_m_tiles;
   size_t route_scratch;  // int32 [chunks][E + 1] for the multi-CTA routing
+  // With the combine fused into GEMM2 only (0 otherwise): int32
+  // [T][combine_stride], per token the number of valid slots, then one
+  // arrival counter per (GEMM2 n tile, column half).
+  size_t combine_cnt;
+  int combine_stride;
 };
 
 // Number of routing chunks for S slots (0: the single-CTA kernel is used).
@@ -88,9 +102,19 @@ cudaError_t launch_kernel(bool dependent, void (*kern)(KArgs...), dim3 grid, dim
 cudaError_t launch_route(const int32_t* topk_idx, int S, int E, const WsLayout& L, uint8_t* ws, cudaStream_t st);
 cudaError_t launch_quant(const void* hidden, int T, int H, int K, const WsLayout& L, uint8_t* ws, cudaStream_t st);
 // Routing + quantization in one launch, for S = T * K <= kFusedRouteQuantSlots.
+// With the fused combine (below) it also sets that up: per-token valid-slot
+// counts, zeroed arrival counters, and the +0 output rows of tokens whose
+// slots are all skipped.
 constexpr int kFusedRouteQuantSlots = 256;
 cudaError_t launch_route_quant_small(const int32_t* topk_idx, const void* hidden, int T, int H, int E, int K,
-                                     const WsLayout& L, uint8_t* ws, cudaStream_t st);
+                                     const WsLayout& L, uint8_t* ws, void* out, cudaStream_t st);
+// The top-k combine fused into GEMM2's epilogue: decode mode with the fused
+// routing + quantization front end. At larger decode batches the separate
+// combine kernel is faster (the epilogue's combines then hold up the
+// accumulator hand-back).
+inline bool fused_combine(int fmt, long long S, int E) {
+  return decode_mode(fmt, S, E) && S <= kFusedRouteQuantSlots;
+}
 cudaError_t launch_combine(const float* y, const int32_t* inv, int T, int H, int K, void* out, cudaStream_t st);
 // transposed: the weights are stored [E][K][N] (N contiguous) instead of [E][N][K].
 cudaError_t launch_prepare(int fmt, bool transposed, int E, int H, int I, const void* w13, const void* w13s,
@@ -114,6 +138,14 @@ struct GemmArgs {
   int out_blocks;             // GEMM1: act_blocks
   int E, I, H;
   int M;                      // padded row capacity (locates the chunk work list)
+  // GEMM2 in decode mode with the fused combine (combine_cnt non-null): the
+  // last arriving row of a token sums the token's rows in ascending k and
+  // writes the bf16 output row
+  const int32_t* inv;         // [T][K] slot -> padded row, -1 skipped
+  int32_t* combine_cnt;       // [T][combine_stride]; null: no fused combine
+  int combine_stride;
+  int K;
+  __nv_bfloat16* out;         // bf16 [T][H]
   float swiglu_limit;         // > 0 and finite: clamp
   GemmGeom g;
 };
@@ -125,9 +157,7 @@ moe_status forward_impl(const void* hidden, const int32_t* topk_idx, const float
                         void* workspace, size_t workspace_bytes, void* out, void* stream, void* const* events);
 
 // decode: FP4 only; 32-row token chunks, activation tensor maps with a
-// 32-row box (tile mode: 128-row m-tiles, 128-row box). Chosen when the
-// pairs per expert average at most kDecodePairsPerExpert.
-constexpr int kDecodePairsPerExpert = 8;
+// 32-row box (tile mode: 128-row m-tiles, 128-row box); see decode_mode().
 cudaError_t launch_gemm(int fmt, bool is_gemm1, bool decode, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                         const GemmArgs& args, int num_sms, cudaStream_t st);
 

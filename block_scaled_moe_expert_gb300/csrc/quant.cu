@@ -82,6 +82,18 @@ __device__ __forceinline__ void quantize_token(const __nv_bfloat16* __restrict__
   }
 }
 
+// Per-token setup of the top-k combine fused into GEMM2's epilogue. The number of valid slots, zeroed arrival counters, and the +0
+// output row of a token whose slots are all skipped (no GEMM2 tile reaches it).
+__device__ __forceinline__ void setup_combine(int t, int n, int32_t* __restrict__ cnt, int stride,
+                                              __nv_bfloat16* __restrict__ out, int H) {
+  int32_t* c = cnt + static_cast<size_t>(t) * stride;
+  for (int i = threadIdx.x; i < stride; i += blockDim.x) c[i] = (i == 0) ? n : 0;
+  if (n == 0) {
+    uint4* o = reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * H);
+    for (int i = threadIdx.x; i < H / 8; i += blockDim.x) o[i] = make_uint4(0, 0, 0, 0);
+  }
+}
+
 // One CTA per token: gathers the token's valid slots from inv (in ascending
 // k) and quantizes the row into each of their padded rows.
 __global__ void __launch_bounds__(kQuantWarps * 32)
@@ -131,7 +143,8 @@ route_quant_small_kernel(const int32_t* __restrict__ idx, const __nv_bfloat16* _
                          int K, int H, int Kp, int M, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                          int32_t* __restrict__ padded_offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
                          int32_t* __restrict__ row_slot, int32_t* __restrict__ tiles, uint32_t* __restrict__ status,
-                         uint8_t* __restrict__ xq, uint32_t* __restrict__ xsf) {
+                         uint8_t* __restrict__ xq, uint32_t* __restrict__ xsf, int32_t* __restrict__ comb_cnt,
+                         int comb_stride, __nv_bfloat16* __restrict__ out) {
   constexpr int kThreads = kQuantWarps * 32;
   __shared__ int key[kFusedRouteQuantSlots];
   __shared__ int rank[kFusedRouteQuantSlots];
@@ -263,6 +276,7 @@ route_quant_small_kernel(const int32_t* __restrict__ idx, const __nv_bfloat16* _
     nrows = n;
   }
   __syncthreads();
+  if (comb_cnt != nullptr) setup_combine(t, nrows, comb_cnt, comb_stride, out, H);
   if (nrows == 0) return;
   quantize_token(hidden + static_cast<size_t>(t) * H, H, Kp, rows, nrows, xq, xsf);
 }
@@ -277,7 +291,7 @@ cudaError_t launch_quant(const void* hidden, int T, int H, int K, const WsLayout
 }
 
 cudaError_t launch_route_quant_small(const int32_t* topk_idx, const void* hidden, int T, int H, int E, int K,
-                                     const WsLayout& L, uint8_t* ws, cudaStream_t st) {
+                                     const WsLayout& L, uint8_t* ws, void* out, cudaStream_t st) {
   const moe_workspace_layout& p = L.pub;
   // The first kernel of the forward is an ordinary launch: it follows
   // whatever the caller queued on the stream.
@@ -287,7 +301,9 @@ cudaError_t launch_route_quant_small(const int32_t* topk_idx, const void* hidden
                        reinterpret_cast<int32_t*>(ws + p.padded_offsets), reinterpret_cast<int32_t*>(ws + p.perm),
                        reinterpret_cast<int32_t*>(ws + p.inv), reinterpret_cast<int32_t*>(ws + p.row_slot),
                        reinterpret_cast<int32_t*>(ws + p.tiles), reinterpret_cast<uint32_t*>(ws + p.status),
-                       ws + p.xq, reinterpret_cast<uint32_t*>(ws + p.xsf));
+                       ws + p.xq, reinterpret_cast<uint32_t*>(ws + p.xsf),
+                       L.combine_cnt ? reinterpret_cast<int32_t*>(ws + L.combine_cnt) : nullptr, L.combine_stride,
+                       reinterpret_cast<__nv_bfloat16*>(out));
 }
 
 }  // namespace bsmoe

@@ -166,3 +166,25 @@ def test_fp4_decode_mode_expert_with_four_chunks():
     r = P.run_cuda(wl, idx=idx, w=w)
     ref = P.oracle_out(r["hidden"], r["idx"], r["w"], r["weights"], wl.swiglu_limit)
     P.assert_close(r["out"], ref, "four chunks")
+
+
+def test_fp4_fused_combine_matches_the_combine_kernel():
+    """FP4 decode batches of at most 256 slots sum each token's rows in GEMM2's
+    epilogue; the same tokens in a larger decode batch go through the separate
+    combine kernel. Same bits either way, +0 rows for tokens whose slots are
+    all skipped, and H = 320 ends halfway through a 128-column half."""
+    wl = W.Workload("fp4_fused_combine", 30, 320, 192, 64, 4, "fp4", "zipf_sigmoid", seed=28, skip_frac=0.3)
+    idx, w = W.make_routing(wl, "cuda")
+    idx[3] = -1
+    idx[17] = -1
+    r = P.run_cuda(wl, idx=idx, w=w)
+    ref = P.oracle_out(r["hidden"], r["idx"], r["w"], r["weights"], None)
+    P.assert_close(r["out"], ref, "fused combine")
+    assert (r["out"][3].view(torch.int16) == 0).all() and (r["out"][17].view(torch.int16) == 0).all()
+    extra = 40  # 70 tokens x 4 = 280 slots: still decode mode, separate combine
+    g = torch.Generator(device="cuda").manual_seed(6)
+    hid = torch.cat([r["hidden"], torch.randn(extra, wl.H, generator=g, device="cuda").to(torch.bfloat16)])
+    idx2 = torch.cat([idx, torch.randint(0, wl.E, (extra, wl.K), generator=g, device="cuda", dtype=torch.int32)])
+    w2 = torch.cat([w, torch.rand(extra, wl.K, generator=g, device="cuda")])
+    out = P.B.experts_forward(hid, idx2, w2, r["prepared"])
+    assert torch.equal(out[:wl.T].view(torch.int16), r["out"].view(torch.int16))

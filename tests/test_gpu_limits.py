@@ -17,6 +17,9 @@ CASES = [
     W.Workload("e512_k32", 64, 256, 128, 512, 32, "fp8", "softmax", seed=61),
     # 32 slots per token over 9600 slots: the multi-CTA routing path, FP4
     W.Workload("k32_multicta_fp4", 300, 256, 128, 40, 32, "fp4", "zipf_sigmoid", seed=62, skip_frac=0.05),
+    # 32 slots per token in an FP4 decode batch of 256 slots: the combine fused
+    # into GEMM2 sums 32 rows per token
+    W.Workload("k32_fused_combine_fp4", 8, 256, 128, 40, 32, "fp4", "softmax", seed=65),
     # H = 32768: GEMM1 runs 256 K blocks, GEMM2 128 N tiles
     W.Workload("h32768_fp8", 40, 32768, 128, 2, 1, "fp8", "softmax", seed=63),
     # I = 32768: GEMM1 runs 256 N tiles, GEMM2 256 K blocks
