@@ -207,8 +207,63 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = sm.tmem_base;
+  // FP4 stage bytes: the tile lands unpacked (16 codes per 16 bytes) but the
+  // copy's transaction count is the packed global size.
+  constexpr uint32_t kStageBytes = (FMT == MOE_W_FP4)
+                                       ? Pipe<DEC>::kAStride + kTileBBytes / 2 + kSfaBytes + kSfbBytes
+                                       : Pipe<DEC>::kAStride + kTileBBytes;
+  // Decode mode: the weight tiles (and their scale blocks) of the first
+  // stages of this CTA's first unit are loaded before the dependency wait,
+  // while the previous kernel still runs; only the activation side waits.
+  // GEMM2 reads the unit from the routing tables (complete: every GEMM1 CTA
+  // passed its own wait before this grid could start); GEMM1 derives it from
+  // the top-k ids, where at most 32 slots give each touched expert one chunk
+  // and chunks follow ascending expert id.
+  int pre_unit = -1, pre_n = 0;
+  if constexpr (DEC) {
+    if (warp == 0) {
+      int e = -1, nt = 0;
+      if constexpr (GEMM1) {
+        if (args.topk_idx != nullptr) {
+          const int id = lane < args.S ? __ldg(args.topk_idx + lane) : -1;
+          const bool valid = id >= 0 && id < args.E;
+          const unsigned same = __match_any_sync(0xffffffffu, valid ? id : (0x40000000 | lane));
+          const bool first = valid && (__ffs(same) - 1 == lane);
+          const unsigned firsts = __ballot_sync(0xffffffffu, first);
+          int rank = 0;  // distinct touched experts below this one
+          for (int j = 0; j < 32; ++j) {
+            const int idj = __shfl_sync(0xffffffffu, id, j);
+            if ((firsts >> j) & 1u) rank += (idj < id);
+          }
+          const int ci = static_cast<int>(blockIdx.x) / NT;
+          if (ci < __popc(firsts)) {
+            const unsigned sel = __ballot_sync(0xffffffffu, first && rank == ci);
+            e = __shfl_sync(0xffffffffu, id, __ffs(sel) - 1);
+            nt = static_cast<int>(blockIdx.x) - ci * NT;
+          }
+        }
+      } else {
+        if (static_cast<int>(blockIdx.x) < __ldg(args.tiles + 1) * NT) {
+          const TileCoord c = tile_of(blockIdx.x);
+          e = c.e;
+          nt = c.nt;
+        }
+      }
+      if (lane == 0 && e >= 0) {
+        pre_unit = blockIdx.x;
+        pre_n = min(kStages, KB);
+        const int wrow = e * g.Np + nt * kBlockN;
+        for (int s = 0; s < pre_n; ++s) {
+          mbar_arrive_expect_tx(&sm.full[s], kStageBytes);
+          tma_load_2d(sm.b[s], &tmap_b, &sm.full[s], s * kBlockK, wrow);
+          bulk_load(sm.sfb[s], args.w_scale + ((static_cast<size_t>(e) * NT + nt) * KB + s) * kSfbBytes, kSfbBytes,
+                    &sm.full[s]);
+        }
+      }
+    }
+  }
   // Everything above overlaps the previous kernel's tail; the tile list and
-  // the operands are written by the kernels before this one.
+  // the activations are written by the kernels before this one.
   pdl_wait();
   pdl_launch_dependents();
   const int total_tiles = __ldg(args.tiles + (DEC ? 1 : 0)) * NT;
@@ -220,10 +275,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
     if (lane == 0) {
       tma_prefetch_desc(&tmap_a);
       tma_prefetch_desc(&tmap_b);
-      // The FP4 tile lands unpacked (16 codes per 16 bytes) but the copy's
-      // transaction count is the packed global size.
-      constexpr uint32_t kA = Pipe<DEC>::kAStride;
-      const uint32_t bytes = (FMT == MOE_W_FP4) ? kA + kTileBBytes / 2 + kSfaBytes + kSfbBytes : kA + kTileBBytes;
       int stage = 0;
       uint32_t phase = 0;
       for (int idx = blockIdx.x; idx < total_tiles && !*abort_flag; idx += gridDim.x) {
@@ -231,15 +282,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
         const int wrow = c.e * g.Np + c.nt * kBlockN;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(&sm.empty[stage], phase ^ 1, abort_flag)) break;
-          mbar_arrive_expect_tx(&sm.full[stage], bytes);
+          // weights already in flight from before the dependency wait
+          const bool pre = idx == pre_unit && kb < pre_n;
+          if (!pre) mbar_arrive_expect_tx(&sm.full[stage], kStageBytes);
           tma_load_2d(sm.a_stage(stage), &tmap_a, &sm.full[stage], kb * kBlockK, c.row0);
-          tma_load_2d(sm.b[stage], &tmap_b, &sm.full[stage], kb * kBlockK, wrow);
+          if (!pre) tma_load_2d(sm.b[stage], &tmap_b, &sm.full[stage], kb * kBlockK, wrow);
           if constexpr (FMT == MOE_W_FP4) {
             bulk_load(sm.sfa[stage], args.a_sf + (static_cast<size_t>(c.row0 / kBlockM) * KB + kb) * kSfaBytes,
                       kSfaBytes, &sm.full[stage]);
-            bulk_load(sm.sfb[stage],
-                      args.w_scale + ((static_cast<size_t>(c.e) * NT + c.nt) * KB + kb) * kSfbBytes, kSfbBytes,
-                      &sm.full[stage]);
+            if (!pre)
+              bulk_load(sm.sfb[stage],
+                        args.w_scale + ((static_cast<size_t>(c.e) * NT + c.nt) * KB + kb) * kSfbBytes, kSfbBytes,
+                        &sm.full[stage]);
           }
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }

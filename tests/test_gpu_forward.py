@@ -188,3 +188,30 @@ def test_fp4_fused_combine_matches_the_combine_kernel():
     w2 = torch.cat([w, torch.rand(extra, wl.K, generator=g, device="cuda")])
     out = P.B.experts_forward(hid, idx2, w2, r["prepared"])
     assert torch.equal(out[:wl.T].view(torch.int16), r["out"].view(torch.int16))
+
+
+@pytest.mark.parametrize("T,K,E", [(1, 8, 64), (3, 8, 40), (8, 4, 16)])
+def test_fp4_decode_first_units_from_the_topk_ids(T, K, E):
+    """FP4 decode batches of at most 32 slots: each GEMM1 CTA finds its first
+    unit from the top-k ids (before the routing kernel completes) to start its
+    weight loads early. Duplicate ids, skipped slots and an all-skipped token
+    must give the same bits as the same tokens inside a larger batch, where
+    the units come from the routing tables only, and match the oracle."""
+    wl = W.Workload(f"fp4_first_units_T{T}", T, 512, 256, E, K, "fp4", "zipf_sigmoid", seed=30 + T)
+    idx, w = W.make_routing(wl, "cuda")
+    idx[0, 1] = idx[0, 0]  # duplicate id in one token
+    idx[0, 2] = -1
+    if T > 2:
+        idx[1] = -1  # all slots skipped
+        idx[2, 0] = E - 1
+    r = P.run_cuda(wl, idx=idx, w=w)
+    ref = P.oracle_out(r["hidden"], r["idx"], r["w"], r["weights"], None)
+    P.assert_close(r["out"], ref, wl.name)
+    assert P.B.device_status(r["ws"]) == 0
+    extra = 40 // K + 1  # pushes the batch past 32 slots
+    g = torch.Generator(device="cuda").manual_seed(7)
+    hid = torch.cat([r["hidden"], torch.randn(extra, wl.H, generator=g, device="cuda").to(torch.bfloat16)])
+    idx2 = torch.cat([idx, torch.randint(0, E, (extra, K), generator=g, device="cuda", dtype=torch.int32)])
+    w2 = torch.cat([w, torch.rand(extra, K, generator=g, device="cuda")])
+    out = P.B.experts_forward(hid, idx2, w2, r["prepared"])
+    assert torch.equal(out[:T].view(torch.int16), r["out"].view(torch.int16))
