@@ -329,10 +329,6 @@ moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, cons
   a1.out_cols = g2.Kp;
   a1.out_blocks = g2.KB;
   a1.g = g1;
-  if (decode && L.S <= kChunkRows) {
-    a1.topk_idx = topk_idx;
-    a1.S = static_cast<int>(L.S);
-  }
   if (launch_gemm(fmt, true, decode, ta1, tb1, a1, d.sms, st) != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;
 
   GemmArgs a2 = a;

@@ -212,53 +212,24 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
   constexpr uint32_t kStageBytes = (FMT == MOE_W_FP4)
                                        ? Pipe<DEC>::kAStride + kTileBBytes / 2 + kSfaBytes + kSfbBytes
                                        : Pipe<DEC>::kAStride + kTileBBytes;
-  // Decode mode: the weight tiles (and their scale blocks) of the first
+  // Decode-mode GEMM2: the weight tiles (and their scale blocks) of the first
   // stages of this CTA's first unit are loaded before the dependency wait,
-  // while the previous kernel still runs; only the activation side waits.
-  // GEMM2 reads the unit from the routing tables (complete: every GEMM1 CTA
-  // passed its own wait before this grid could start); GEMM1 derives it from
-  // the top-k ids, where at most 32 slots give each touched expert one chunk
-  // and chunks follow ascending expert id.
+  // while GEMM1 drains; only the activation side waits. The unit comes from
+  // the routing tables, which are complete: this grid cannot start before
+  // every GEMM1 CTA has passed its own wait, i.e. before the routing kernel
+  // has finished.
   int pre_unit = -1, pre_n = 0;
-  if constexpr (DEC) {
-    if (warp == 0) {
-      int e = -1, nt = 0;
-      if constexpr (GEMM1) {
-        if (args.topk_idx != nullptr) {
-          const int id = lane < args.S ? __ldg(args.topk_idx + lane) : -1;
-          const bool valid = id >= 0 && id < args.E;
-          const unsigned same = __match_any_sync(0xffffffffu, valid ? id : (0x40000000 | lane));
-          const bool first = valid && (__ffs(same) - 1 == lane);
-          const unsigned firsts = __ballot_sync(0xffffffffu, first);
-          int rank = 0;  // distinct touched experts below this one
-          for (int j = 0; j < 32; ++j) {
-            const int idj = __shfl_sync(0xffffffffu, id, j);
-            if ((firsts >> j) & 1u) rank += (idj < id);
-          }
-          const int ci = static_cast<int>(blockIdx.x) / NT;
-          if (ci < __popc(firsts)) {
-            const unsigned sel = __ballot_sync(0xffffffffu, first && rank == ci);
-            e = __shfl_sync(0xffffffffu, id, __ffs(sel) - 1);
-            nt = static_cast<int>(blockIdx.x) - ci * NT;
-          }
-        }
-      } else {
-        if (static_cast<int>(blockIdx.x) < __ldg(args.tiles + 1) * NT) {
-          const TileCoord c = tile_of(blockIdx.x);
-          e = c.e;
-          nt = c.nt;
-        }
-      }
-      if (lane == 0 && e >= 0) {
-        pre_unit = blockIdx.x;
-        pre_n = min(kStages, KB);
-        const int wrow = e * g.Np + nt * kBlockN;
-        for (int s = 0; s < pre_n; ++s) {
-          mbar_arrive_expect_tx(&sm.full[s], kStageBytes);
-          tma_load_2d(sm.b[s], &tmap_b, &sm.full[s], s * kBlockK, wrow);
-          bulk_load(sm.sfb[s], args.w_scale + ((static_cast<size_t>(e) * NT + nt) * KB + s) * kSfbBytes, kSfbBytes,
-                    &sm.full[s]);
-        }
+  if constexpr (DEC && !GEMM1) {
+    if (tid == 0 && static_cast<int>(blockIdx.x) < __ldg(args.tiles + 1) * NT) {
+      const TileCoord c = tile_of(blockIdx.x);
+      pre_unit = blockIdx.x;
+      pre_n = min(kStages, KB);
+      const int wrow = c.e * g.Np + c.nt * kBlockN;
+      for (int s = 0; s < pre_n; ++s) {
+        mbar_arrive_expect_tx(&sm.full[s], kStageBytes);
+        tma_load_2d(sm.b[s], &tmap_b, &sm.full[s], s * kBlockK, wrow);
+        bulk_load(sm.sfb[s], args.w_scale + ((static_cast<size_t>(c.e) * NT + c.nt) * KB + s) * kSfbBytes, kSfbBytes,
+                  &sm.full[s]);
       }
     }
   }

@@ -146,10 +146,6 @@ struct GemmArgs {
   int combine_stride;
   int K;
   __nv_bfloat16* out;         // bf16 [T][H]
-  // GEMM1 in decode mode with S <= 32 slots (else null): the top-k ids, from
-  // which each CTA finds its first unit before the routing kernel completes
-  const int32_t* topk_idx;
-  int S;
   float swiglu_limit;         // > 0 and finite: clamp
   GemmGeom g;
 };

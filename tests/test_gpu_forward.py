@@ -191,12 +191,11 @@ def test_fp4_fused_combine_matches_the_combine_kernel():
 
 
 @pytest.mark.parametrize("T,K,E", [(1, 8, 64), (3, 8, 40), (8, 4, 16)])
-def test_fp4_decode_first_units_from_the_topk_ids(T, K, E):
-    """FP4 decode batches of at most 32 slots: each GEMM1 CTA finds its first
-    unit from the top-k ids (before the routing kernel completes) to start its
-    weight loads early. Duplicate ids, skipped slots and an all-skipped token
-    must give the same bits as the same tokens inside a larger batch, where
-    the units come from the routing tables only, and match the oracle."""
+def test_fp4_small_decode_batches_match_larger_batches(T, K, E):
+    """FP4 decode batches of at most 32 slots (GEMM2 starts its first weight
+    copies before waiting for GEMM1): duplicate ids, skipped slots and an
+    all-skipped token give the same bits as the same tokens inside a larger
+    batch, and match the oracle."""
     wl = W.Workload(f"fp4_first_units_T{T}", T, 512, 256, E, K, "fp4", "zipf_sigmoid", seed=30 + T)
     idx, w = W.make_routing(wl, "cuda")
     idx[0, 1] = idx[0, 0]  # duplicate id in one token
