@@ -58,25 +58,37 @@ def dist_env():
     return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def kernel_source_digest(sources):
+    """sha256 over the GEMM kernel sources with comments and whitespace
+    removed (edits to comments do not change what was measured); None if a
+    file is missing."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for src in sources:
+        try:
+            with open(os.path.join(ROOT, src), encoding="utf-8") as f:
+                text = f.read()
+        except OSError:
+            return None
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update("".join(text.split()).encode())
+    return h.hexdigest()
+
+
 def measured_traffic(workload, kernel):
     """DRAM bytes per launch from the committed ncu summary, or None when the
     GEMM kernel sources changed since the counters were taken."""
     import glob
-    import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "dram_traffic_full_size.json")) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    h = hashlib.sha256()
-    for src in d.get("sources", []):
-        try:
-            with open(os.path.join(ROOT, src), "rb") as f:
-                h.update(f.read())
-        except OSError:
-            return None
+    digest = kernel_source_digest(d.get("sources", []))
     cur = sorted(glob.glob(os.path.join(ROOT, "block_scaled_moe_expert_gb300", "csrc", "*.cuh")))
-    if len(cur) + 1 != len(d.get("sources", [])) or h.hexdigest() != d.get("kernel_source_sha256"):
+    if digest is None or len(cur) + 1 != len(d.get("sources", [])) or digest != d.get("kernel_source_sha256"):
         return None
     return d.get("bytes_per_launch", {}).get(workload, {}).get(kernel)
 

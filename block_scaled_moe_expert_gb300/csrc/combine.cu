@@ -1,6 +1,8 @@
 // Deterministic gather-combine of the weighted per-pair rows.
 //
-// "fp8_grouped_mm_experts_forward" (finegrained_fp8.py excerpt) zeroes the
+// fp8_grouped_mm_experts_forward (source excerpt on the error page
+// "grouped_mm experts dispatch does not support activation_scheme='static'")
+// zeroes the
 // sentinel rows and then reduces the top-k rows of each token with
 // view(T, K, H).sum(1) instead of index_add_, because atomicAdd with
 // duplicate indices is non-deterministic; the result is cast back to the

@@ -1,8 +1,9 @@
 // Grouped block-scaled GEMMs of the experts forward on tcgen05 tensor cores.
 //
-// The deepgemm excerpt (deepgemm.py lines 678-714) runs the experts as two
-// grouped matmuls with FP8 activations and FP8 or FP4 expert weights
-// (grouped_fp8_fp4_matmul_nt: both operands K-major). This kernel computes,
+// The error record "DeepGEMM experts selected on a model spanning multiple
+// CUDA devices" (source excerpt of deepgemm_fp8_fp4_experts_forward) runs the
+// experts as two grouped matmuls with FP8 activations and FP8 or FP4 expert
+// weights (grouped_fp8_fp4_matmul_nt: both operands K-major). This kernel computes,
 // for every expert e and every 128-row tile of its group in the padded
 // grouped layout, one 128 x 256 output tile:
 //
@@ -13,13 +14,17 @@
 // Mega MoE docstring), act = silu(gate) * up in fp32, requantization of act
 // in 1x128 blocks with the same power-of-two e4m3 rule as the input.
 // GEMM2 (A = act, W = down_proj) multiplies each row by the routing weight of
-// its slot and stores fp32 rows for the deterministic combine.
+// its slot and stores fp32 rows for the deterministic combine (in the FP4
+// decode mode with at most 256 slots it also performs that combine).
 //
 // Pipeline (one persistent CTA per SM, 12 warps):
-//   warp 0      TMA producer: A tile 128x128 B, W tile 256x128 B (+ FP4 scale
-//               blocks) per 128-K stage into a 4-deep shared-memory ring;
-//   warp 1      allocates tensor memory and issues tcgen05.mma (one thread);
-//   warps 2, 3  idle;
+//   warp 0      TMA producer: A tile 128x128 B (decode mode: a 32-row chunk),
+//               W tile 256x128 B (+ FP4 scale blocks) per 128-K stage into a
+//               4-deep (decode mode: 5-deep) shared-memory ring;
+//   warp 1      allocates tensor memory and issues tcgen05.mma (one thread;
+//               the whole warp in decode mode);
+//   warp 2      FP8: producer of the promotion scales; FP4: idle;
+//   warp 3      idle;
 //   warps 4..11 two epilogue warpgroups, each owning 128 of the 256 columns.
 // The first warpgroup hands registers to the epilogue warpgroups with
 // setmaxnreg (launch: 384 x 168; after: 128 x 56 + 256 x 224 = 64512).

@@ -1,6 +1,8 @@
 // One-shot weight transform into the kernel layout.
 //
-// The Mega MoE forward (deepgemm.py error page, lines 857-893) packs the
+// The Mega MoE forward (source excerpt on the error pages "DeepGEMM Mega MoE
+// requires a process_group for the EP group" and "... requires FP4-packed
+// expert weights") packs the
 // UE8M0 scale factors and interleaves the L1/L2 weights once, before the
 // first forward. This is the same idea made explicit:
 //   * gate_up rows are interleaved in 64-row groups so that one 256-row

@@ -1,9 +1,10 @@
 // Dynamic 1x128 activation quantization fused with the padded permute.
 //
 // The grouped experts dispatch quantizes activations dynamically per block
-// (finegrained_fp8.py error page, "What it means"); rows are then gathered by
-// slot // K into the grouped layout ("fp8_grouped_mm_experts_forward",
-// finegrained_fp8.py excerpt). Each token is quantized once and its bytes are
+// (error page "grouped_mm experts dispatch does not support
+// activation_scheme='static'", section "What it means"); rows are then
+// gathered by slot // K into the grouped layout (fp8_grouped_mm_experts_forward,
+// the source excerpt on the same page). Each token is quantized once and its bytes are
 // copied to the padded row of every valid slot of that token, which equals
 // quantizing the gathered rows.
 //

@@ -1,9 +1,12 @@
 // Routing: flatten the top-k pairs, count them per expert and place them in a
 // padded grouped layout with a stable counting sort.
 //
-// Follows "fp8_grouped_mm_experts_forward" (finegrained_fp8.py excerpt):
+// Follows fp8_grouped_mm_experts_forward (source excerpt on the error page
+// "grouped_mm experts dispatch does not support activation_scheme='static'"):
 // flatten (slot s = t*K + k), sort by expert id, gather rows by s // K; and
-// the sorted_to_padded map of the deepgemm excerpt (lines 678-684). The sort
+// the sorted_to_padded map of the deepgemm_fp8_fp4_experts_forward source
+// excerpt (error record "DeepGEMM experts selected on a model spanning
+// multiple CUDA devices"). The sort
 // is stable (equal ids keep ascending slot order) and a skipped slot (-1, or
 // an id outside [-1, E), which also raises MOE_DEV_BAD_EXPERT_ID) takes key E
 // so it sorts after every group.

@@ -4,18 +4,20 @@
  * The operation is the experts half of a Mixture-of-Experts layer as the
  * transformers integration pages describe it:
  *
- *   - "fp8_grouped_mm_experts_forward" (finegrained_fp8.py error page, source
- *     excerpt): flatten the T*K token-expert pairs, sort them by expert,
+ *   - fp8_grouped_mm_experts_forward (source excerpt on the error page
+ *     "grouped_mm experts dispatch does not support activation_scheme='static'"): flatten the T*K token-expert pairs, sort them by expert,
  *     gather hidden rows by slot // K, run the grouped block-scaled matmuls
  *     with activations quantized dynamically per block, zero the sentinel
  *     rows, reduce the top-k rows of each token with a deterministic
  *     reshape+sum (no atomics) and cast back to the input dtype;
- *   - "deepgemm_fp8_fp4_experts_forward" (deepgemm.py error record, excerpt
- *     lines 678-714): grouped FP8-activation x FP8/FP4-weight matmuls over a
+ *   - "deepgemm_fp8_fp4_experts_forward" (source excerpt of the error record
+ *     "DeepGEMM experts selected on a model spanning multiple CUDA devices"):
+ *     grouped FP8-activation x FP8/FP4-weight matmuls over a
  *     padded grouped layout (sorted_to_padded), bf16 hidden states only,
  *     static activation scales refused, one CUDA device per call;
- *   - the DeepGEMM Mega MoE forward docstring (deepgemm.py error page, lines
- *     857-893): top-k ids are GLOBAL expert ids and -1 marks a skipped slot;
+ *   - the DeepGEMM Mega MoE forward docstring (source excerpt of the error
+ *     record "DeepGEMM Mega MoE requires a process_group for the EP group"):
+ *     top-k ids are GLOBAL expert ids and -1 marks a skipped slot;
  *     gate_up / down weights carry UE8M0 scale factors and are transformed
  *     once before the first forward (scale packing and weight interleave);
  *     swiglu_limit is an optional clamp, unclamped when absent.
@@ -128,8 +130,8 @@ moe_status moe_prepare_weights(int fmt, int E, int H, int I, const void* w13, co
 /*
  * The same transform for expert weights stored transposed, N contiguous
  * (the `is_transposed` storage that the experts dispatch serves with
- * grouped_fp8_fp4_matmul_nn instead of _nt, deepgemm.py error record,
- * lines 678-714). Writes exactly the bytes moe_prepare_weights writes for
+ * grouped_fp8_fp4_matmul_nn instead of _nt: the deepgemm_fp8_fp4_experts_forward
+ * source excerpt). Writes exactly the bytes moe_prepare_weights writes for
  * the same weights in the K-major storage, so the forward does not change.
  *
  * Inputs (read only, device):

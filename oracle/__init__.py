@@ -8,17 +8,18 @@ same seeded input bytes.
 
 Sources. The method is spread over a handful of transformers pages:
 
-* "fp8_grouped_mm_experts_forward" (finegrained_fp8.py error page, source
-  excerpt): flatten the top-k pairs, sort them by expert, gather rows by
+* ``fp8_grouped_mm_experts_forward`` (source excerpt on the error page
+  "grouped_mm experts dispatch does not support activation_scheme='static'"): flatten the top-k pairs, sort them by expert, gather rows by
   ``perm // K``; afterwards zero the sentinel rows and reduce the top-k rows
   per token with a deterministic reshape+sum, then cast to the input dtype.
   The same page states that the grouped dispatch quantizes activations
   dynamically per block.
-* "deepgemm_fp8_fp4_experts_forward" (deepgemm.py error record, excerpt
-  lines 678-714): the sorted-to-padded grouped layout, the grouped FP8 x
-  FP8/FP4 matmul, and the bf16-only / static-scheme / multi-device refusals.
-* "DeepGEMM Mega MoE" forward docstring (deepgemm.py error page, lines
-  857-893): top-k ids are global expert ids with -1 marking skipped slots;
+* "deepgemm_fp8_fp4_experts_forward" (source excerpt of the error record
+  "DeepGEMM experts selected on a model spanning multiple CUDA devices"): the
+  sorted-to-padded grouped layout, the grouped FP8 x FP8/FP4 matmul, and the
+  bf16-only / static-scheme / multi-device refusals.
+* "DeepGEMM Mega MoE" forward docstring (source excerpt of the error record
+  "DeepGEMM Mega MoE requires a process_group for the EP group"): top-k ids are global expert ids with -1 marking skipped slots;
   gate_up and down weights carry UE8M0 scale factors; ``swiglu_limit`` is an
   optional clamp, unclamped when absent.
 

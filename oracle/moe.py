@@ -4,7 +4,8 @@ Test infrastructure only (see the package docstring).
 
 Steps, in the order the pages give them:
 1. Flatten the top-k pairs and route them (``oracle.routing``), following
-   "fp8_grouped_mm_experts_forward" (finegrained_fp8.py excerpt).
+   fp8_grouped_mm_experts_forward (source excerpt on the error page
+   "grouped_mm experts dispatch does not support activation_scheme='static'").
 2. Quantize each hidden row dynamically in 1x128 blocks to e4m3 with a
    power-of-two scale ("quantizes activations dynamically per-block", same
    page). A token is quantized once; every pair of the token uses the same

@@ -2,13 +2,16 @@
 
 Test infrastructure only (see the package docstring).
 
-Follows "fp8_grouped_mm_experts_forward" (finegrained_fp8.py error page,
-source excerpt): the S = T*K pairs are flattened in (token, k) order
+Follows ``fp8_grouped_mm_experts_forward`` (source excerpt on the error page
+"grouped_mm experts dispatch does not support activation_scheme='static'"): the S = T*K pairs are flattened in (token, k) order
 (``top_k_index.reshape(-1)``), sorted by expert id (``torch.sort``) and the
-hidden row of slot s is gathered by ``s // K``. The deepgemm excerpt (lines
-678-684) adds a ``sorted_to_padded`` map: each expert's rows start at an
-aligned offset of a padded grouped buffer. The Mega MoE docstring (lines
-857-893) states that ids are global and -1 marks a skipped slot.
+hidden row of slot s is gathered by ``s // K``. The source excerpt of
+``deepgemm_fp8_fp4_experts_forward`` (error record "DeepGEMM experts selected
+on a model spanning multiple CUDA devices") adds a ``sorted_to_padded`` map:
+each expert's rows start at an aligned offset of a padded grouped buffer. The
+Mega MoE forward docstring (source excerpt of the error record "DeepGEMM Mega
+MoE requires a process_group for the EP group") states that ids are global
+and -1 marks a skipped slot.
 
 Readings where the pages are silent:
 * the sort is stable (equal ids keep ascending slot order) and a skipped slot
