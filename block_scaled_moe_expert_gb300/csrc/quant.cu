@@ -26,17 +26,32 @@ namespace {
 
 constexpr int kQuantWarps = 8;
 
+constexpr int kMaxRowBytes = 32768;  // the largest hidden size the library accepts
+
+// Shared -> global bulk copy (both addresses 16-byte aligned, size a
+// multiple of 16), tracked by the issuing thread's bulk group.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_store_commit_and_wait() {
+  asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Quantizes one token row and copies its bytes to the n padded rows listed
 // in `rows`. A warp covers 256 columns (two 128-column blocks) per step: each
-// lane loads 8 bf16 (16 bytes), the 16 lanes of a half-warp reduce the
-// block's amax, and each lane stores 8 code bytes per destination row, so a
-// warp writes 256 contiguous bytes of every row it copies to. The loads of
-// kLoadBatch steps are issued together, so a row (up to 8 x 256 x kLoadBatch
-// columns) costs one memory latency instead of one per step.
+// lane loads 8 bf16 (16 bytes) and the 16 lanes of a half-warp reduce the
+// block's amax. The loads of kLoadBatch steps are issued together, so a row
+// (up to 8 x 256 x kLoadBatch columns) costs one memory latency instead of
+// one per step. The codes and exponent words are assembled in shared memory
+// (`qrow`, `qsf`) and each destination row is written by one bulk copy:
+// writing them with per-lane stores, eight rows of a token took 3-4 µs of
+// store issue alone.
 constexpr int kLoadBatch = 4;
 __device__ __forceinline__ void quantize_token(const __nv_bfloat16* __restrict__ xr, int H, int Kp,
                                                const int* rows, int n, uint8_t* __restrict__ xq,
-                                               uint32_t* __restrict__ xsf) {
+                                               uint32_t* __restrict__ xsf, uint8_t* qrow, uint32_t* qsf) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nblk = Kp / 128;
   constexpr int kStep = kQuantWarps * 256;
@@ -67,20 +82,25 @@ __device__ __forceinline__ void quantize_token(const __nv_bfloat16* __restrict__
       for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
       const int e = act_exponent(amax);
       const float s = exp2_neg(e);
-      const uint2 q = make_uint2(pack4_e4m3(v[0] * s, v[1] * s, v[2] * s, v[3] * s),
-                                 pack4_e4m3(v[4] * s, v[5] * s, v[6] * s, v[7] * s));
-      const uint32_t word = static_cast<uint32_t>(e + 127) * 0x01010101u;
-      const bool in_range = c0 < Kp;
-      const int blk = c0 / 128;
-      for (int i = 0; i < n; ++i) {
-        const int r = rows[i];
-        if (in_range) {
-          *reinterpret_cast<uint2*>(xq + static_cast<size_t>(r) * Kp + c0) = q;
-          if ((lane & 15) == 0) xsf[sf_word_index(r, blk, nblk)] = word;
-        }
+      if (c0 < Kp) {
+        *reinterpret_cast<uint2*>(qrow + c0) = make_uint2(pack4_e4m3(v[0] * s, v[1] * s, v[2] * s, v[3] * s),
+                                                          pack4_e4m3(v[4] * s, v[5] * s, v[6] * s, v[7] * s));
+        if ((lane & 15) == 0) qsf[c0 / 128] = static_cast<uint32_t>(e + 127) * 0x01010101u;
       }
     }
   }
+  fence_proxy_async_smem();  // the bulk copies read qrow through the async proxy
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < n; ++i) bulk_store(xq + static_cast<size_t>(rows[i]) * Kp, qrow, Kp);
+  }
+  // exponent words: scattered in the MMA scale layout, plain stores
+  for (int j = threadIdx.x; j < n * nblk; j += blockDim.x) {
+    const int i = j / nblk, b = j - i * nblk;
+    xsf[sf_word_index(rows[i], b, nblk)] = qsf[b];
+  }
+  // the copies read shared memory until they complete
+  if (threadIdx.x == 0) bulk_store_commit_and_wait();
 }
 
 // Per-token setup of the top-k combine fused into GEMM2's epilogue. The number of valid slots, zeroed arrival counters, and the +0
@@ -103,6 +123,8 @@ quant_permute_kernel(const __nv_bfloat16* __restrict__ hidden, int H, int K, int
   const int t = blockIdx.x;
   __shared__ int rows[kMaxTopK];
   __shared__ int nrows;
+  __shared__ __align__(128) uint8_t qrow[kMaxRowBytes];
+  __shared__ uint32_t qsf[kMaxRowBytes / 128];
   pdl_wait();  // inv comes from the routing kernel
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
@@ -115,7 +137,7 @@ quant_permute_kernel(const __nv_bfloat16* __restrict__ hidden, int H, int K, int
   }
   __syncthreads();
   if (nrows == 0) return;
-  quantize_token(hidden + static_cast<size_t>(t) * H, H, Kp, rows, nrows, xq, xsf);
+  quantize_token(hidden + static_cast<size_t>(t) * H, H, Kp, rows, nrows, xq, xsf, qrow, qsf);
 }
 
 // ---------------------------------------------------------------------------
@@ -158,6 +180,8 @@ route_quant_small_kernel(const int32_t* __restrict__ idx, const __nv_bfloat16* _
   __shared__ int rows[kMaxTopK];
   __shared__ int nrows;
   __shared__ int bad;
+  __shared__ __align__(128) uint8_t qrow[kMaxRowBytes];
+  __shared__ uint32_t qsf[kMaxRowBytes / 128];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, t = blockIdx.x;
   pdl_wait();
   pdl_launch_dependents();
@@ -255,16 +279,16 @@ route_quant_small_kernel(const int32_t* __restrict__ idx, const __nv_bfloat16* _
         inv[s] = -1;
       }
     }
-    // Work lists and padding rows, one thread per expert (at most 256
-    // slots, so few experts have any).
+    // Work lists and padding rows, one warp per touched expert (at most 256
+    // slots, so few experts have any), its lanes writing consecutive entries.
     int32_t* expert_of = tiles + tiles_expert_of(E);
     int32_t* chunk_expert = tiles + tiles_chunk_expert(E, M);
-    for (int e = tid; e < E; e += kThreads) {
+    for (int e = warp; e < E; e += kQuantWarps) {
       const int c = cnt[e];
       if (c == 0) continue;
-      for (int g = mts[e]; g < mts[e + 1]; ++g) expert_of[g] = e;
-      for (int g = chs[e]; g < chs[e + 1]; ++g) chunk_expert[g] = e;
-      for (int r = pad[e] + c; r < pad[e + 1]; ++r) row_slot[r] = -1;  // padding rows
+      for (int g = mts[e] + lane; g < mts[e + 1]; g += 32) expert_of[g] = e;
+      for (int g = chs[e] + lane; g < chs[e + 1]; g += 32) chunk_expert[g] = e;
+      for (int r = pad[e] + c + lane; r < pad[e + 1]; r += 32) row_slot[r] = -1;  // padding rows
     }
   }
 
@@ -279,7 +303,7 @@ route_quant_small_kernel(const int32_t* __restrict__ idx, const __nv_bfloat16* _
   __syncthreads();
   if (comb_cnt != nullptr) setup_combine(t, nrows, comb_cnt, comb_stride, out, H);
   if (nrows == 0) return;
-  quantize_token(hidden + static_cast<size_t>(t) * H, H, Kp, rows, nrows, xq, xsf);
+  quantize_token(hidden + static_cast<size_t>(t) * H, H, Kp, rows, nrows, xq, xsf, qrow, qsf);
 }
 
 }  // namespace
