@@ -266,13 +266,18 @@ def run_reference(args, wl):
             pairs.append(routing_stats(ids[t:t + 1], wl.E)[0])
     total = sum(times)
     flops = 6.0 * wl.H * wl.I * sum(pairs)
+    # the same config keys as the GPU arm, from the host-generated full batch
+    full_pairs, full_touched = routing_stats(W.make_routing(wl)[0].numpy(), wl.E)
     value = flops / total / 1e12
     cores = len(os.sched_getaffinity(0))
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
-                                            "K": wl.K, "weights": wl.fmt},
+            "data": "synthetic",
+            "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "K": wl.K,
+                       "weights": wl.fmt, "swiglu_limit": wl.swiglu_limit, "pairs": full_pairs,
+                       "touched_experts": full_touched, "parallelism": f"replicas{ws}",
+                       "l2": "not applicable: the oracle runs on the host"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": f"one token of {wl.name} per step (synthetic expert weights), fp64 numpy"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

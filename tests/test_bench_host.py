@@ -1,0 +1,107 @@
+"""CPU: host logic of bench.py.
+
+* the number of kernel launches a forward makes (bench.py reports it as
+  gpu_launches) follows the thresholds compiled into the library;
+* the digest that keys the committed DRAM-traffic record ignores comments
+  and whitespace but not code, and is None when a source is missing;
+* the algorithmic weight bytes per expert, against sizes worked out by hand
+  from the two weight formats;
+* the reference arm (`--impl reference`, the oracle on the host) prints one
+  JSON line with the contract's keys and the GPU arm's config keys.
+"""
+import json
+import os
+import re
+import subprocess
+import sys
+
+import bench
+from block_scaled_moe_expert_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+CSRC = os.path.join(ROOT, "block_scaled_moe_expert_gb300", "csrc")
+
+
+def _const(name, fname):
+    m = re.search(rf"constexpr int {name} = (\d+);", open(os.path.join(CSRC, fname)).read())
+    assert m, name
+    return int(m.group(1))
+
+
+def test_launch_count_follows_the_library_thresholds():
+    fused = _const("kFusedRouteQuantSlots", "moe_internal.cuh")
+    per_expert = _const("kDecodePairsPerExpert", "moe_internal.cuh")
+    single = _const("kSingleCtaSlots", "route.cu")
+
+    def wl(T, K, E, fmt):
+        return W.Workload("case", T, 256, 128, E, K, fmt, "softmax", seed=1)
+
+    # routing + quantization: one fused kernel, then routing + quant, then
+    # histogram + scan + scatter + quant
+    assert bench.launches_per_forward(wl(fused, 1, 8, "fp8")) == 1 + 2 + 1
+    assert bench.launches_per_forward(wl(fused + 1, 1, 8, "fp8")) == 2 + 2 + 1
+    assert bench.launches_per_forward(wl(single, 1, 8, "fp8")) == 2 + 2 + 1
+    assert bench.launches_per_forward(wl(single + 1, 1, 8, "fp8")) == 4 + 2 + 1
+    # FP4 decode mode (at most per_expert pairs per expert) with at most
+    # `fused` slots: the combine runs inside GEMM2
+    E = fused // per_expert
+    assert bench.launches_per_forward(wl(fused, 1, E, "fp4")) == 1 + 2
+    assert bench.launches_per_forward(wl(fused, 1, E, "fp8")) == 1 + 2 + 1
+    assert bench.launches_per_forward(wl(fused, 1, E - 1, "fp4")) == 1 + 2 + 1  # not decode mode
+    assert bench.launches_per_forward(wl(fused + 1, 1, 4 * E, "fp4")) == 2 + 2 + 1  # decode, separate combine
+    # every named workload is one of these cases
+    for name, w in W.WORKLOADS.items():
+        S = w.T * w.K
+        front = 1 if S <= fused else (2 if S <= single else 4)
+        fused_combine = w.fmt == "fp4" and S <= per_expert * w.E and S <= fused
+        assert bench.launches_per_forward(w) == front + 2 + (0 if fused_combine else 1), name
+
+
+def test_traffic_digest_ignores_comments_but_not_code(tmp_path, monkeypatch):
+    src = "block_scaled_moe_expert_gb300/csrc/gemm.cu"
+    text = open(os.path.join(ROOT, src)).read()
+    d = tmp_path / "block_scaled_moe_expert_gb300" / "csrc"
+    d.mkdir(parents=True)
+    f = d / "gemm.cu"
+    f.write_text(text)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    base = bench.kernel_source_digest([src])
+    assert base is not None
+    f.write_text(text.replace("// Grouped block-scaled GEMMs", "//   Grouped   GEMMs, reworded") +
+                 "\n/* a trailing\n   block comment */\n\n")
+    assert bench.kernel_source_digest([src]) == base
+    needle = "kStages = DEC ? 5 : 4"
+    assert needle in text
+    f.write_text(text.replace(needle, "kStages = DEC ? 5 : 3"))
+    assert bench.kernel_source_digest([src]) != base
+    f.unlink()
+    assert bench.kernel_source_digest([src]) is None
+
+
+def test_weight_bytes_per_expert_by_hand():
+    mix = W.WORKLOADS["mixtral_prefill_fp8"]  # H 4096, I 14336, FP8 + fp32 per 128x128
+    assert bench.weight_bytes_per_expert(mix, 13) == 28672 * 4096 + 4 * 224 * 32
+    assert bench.weight_bytes_per_expert(mix, 2) == 4096 * 14336 + 4 * 32 * 112
+    oss = W.WORKLOADS["gptoss_fp8xfp4"]  # H = I = 2880, FP4 + one byte per 1x32
+    assert bench.weight_bytes_per_expert(oss, 13) == 5760 * 1440 + 5760 * 90
+    assert bench.weight_bytes_per_expert(oss, 2) == 2880 * 1440 + 2880 * 90
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                        "tiny_fp8", "--steps", "3", "--warmup", "3"], capture_output=True, text=True, timeout=600,
+                       cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert d["value"] > 0 and d["ms_per_step"] > 0 and d["higher_is_better"] is True
+    assert (d["n_gpus"], d["steps"], d["warmup"], d["vs_baseline"]) == (1, 3, 3, None)
+    assert d["dtype"] == "f64" and d["data"] == "synthetic" and d["scaling"] == "weak"
+    assert set(d["config"]) == {"workload", "T", "H", "I", "E", "K", "weights", "swiglu_limit", "pairs",
+                                "touched_experts", "parallelism", "l2"}
+    assert d["config"]["workload"] == "tiny_fp8" and d["config"]["pairs"] == 32
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
