@@ -55,6 +55,7 @@ _SIGS = {
                                           _vp, _vp]),
     "moe_static_workspace_capacity": (_sz, []),
     "moe_get_device_status": (_int, [_vp, _vp, _c.POINTER(_c.c_uint32)]),
+    "moe_selftest_wait_timeout": (_int, [_vp, _c.c_size_t, _vp]),
     "moe_query_workspace_layout": (_int, [_int, _int, _int, _int, _int, _int, _c.POINTER(MoeLayout)]),
 }
 
@@ -219,6 +220,14 @@ def device_status(workspace):
     return int(flags.value)
 
 
+def selftest_wait_timeout(workspace):
+    """Run the bounded-wait self-test (about one second on the GPU) and
+    return the device flags it left (MOE_DEV_TIMEOUT when the path works)."""
+    _check(lib().moe_selftest_wait_timeout(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                           _stream()), "moe_selftest_wait_timeout")
+    return device_status(workspace)
+
+
 def header_symbols():
     """Names of the functions declared in include/moe_experts.h."""
     import re
@@ -229,4 +238,4 @@ def header_symbols():
 
 __all__ = ["lib", "MoeError", "prepare_weights", "experts_forward", "experts_forward_timed", "experts_forward_static",
            "workspace_bytes", "workspace_layout",
-           "device_status", "PreparedWeights", "header_symbols", "MOE_DEV_BAD_EXPERT_ID", "MOE_DEV_TIMEOUT"]
+           "device_status", "selftest_wait_timeout", "PreparedWeights", "header_symbols", "MOE_DEV_BAD_EXPERT_ID", "MOE_DEV_TIMEOUT"]

@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "moe_internal.cuh"
+#include "ptx.cuh"
 
 namespace bsmoe {
 
@@ -96,6 +97,22 @@ moe_status check_ptr(const void* p, int dev) {
   if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) return MOE_ERR_DEVICE_MISMATCH;
   if (a.device != dev) return MOE_ERR_DEVICE_MISMATCH;
   return MOE_OK;
+}
+
+// Self-test of the bounded-wait path: thread 0 waits, through the helper the
+// GEMM pipeline uses, on an mbarrier phase that nothing completes. The wait
+// gives up after its bound, raises the abort flag, and the kernel reports
+// MOE_DEV_TIMEOUT the way the GEMM does, then returns.
+__global__ void wait_timeout_selftest_kernel(uint32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    const bool done = mbar_wait(&bar, 0, &abort_flag);
+    if (!done && abort_flag) atomicOr(status, MOE_DEV_TIMEOUT);
+  }
 }
 
 }  // namespace
@@ -376,6 +393,17 @@ moe_status moe_experts_forward_timed(const void* hidden, const int32_t* topk_idx
 }  // extern "C"
 
 extern "C" {
+
+moe_status moe_selftest_wait_timeout(void* workspace, size_t workspace_bytes, void* stream) {
+  if (workspace == nullptr || workspace_bytes < sizeof(uint32_t) || reinterpret_cast<uintptr_t>(workspace) % 4)
+    return MOE_ERR_INVALID_ARG;
+  DevInfo d;
+  moe_status s = current_device(&d);
+  if (s != MOE_OK) return s;
+  if ((s = check_ptr(workspace, d.id)) != MOE_OK) return s;
+  wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint32_t*>(workspace));
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
 
 moe_status moe_get_device_status(void* workspace, void* stream, uint32_t* flags) {
   if (workspace == nullptr || flags == nullptr) return MOE_ERR_INVALID_ARG;

@@ -224,6 +224,20 @@ size_t moe_static_workspace_capacity(void);
 moe_status moe_get_device_status(void* workspace, void* stream, uint32_t* flags);
 
 /*
+ * Self-test of the failure path of the pipeline waits. Enqueues on `stream`
+ * one CTA whose thread waits, through the same bounded mbarrier wait the
+ * GEMMs use, on a phase that nothing completes. After its bound (2e9 SM
+ * clock cycles, about one second) the wait gives up and the kernel ORs
+ * MOE_DEV_TIMEOUT into the status word of `workspace` (its first 4 bytes,
+ * device memory of the current device, 4-byte aligned) and returns; the
+ * context stays usable. Read the result with moe_get_device_status.
+ * Returns MOE_ERR_INVALID_ARG for a null, short or misaligned workspace,
+ * MOE_ERR_DEVICE_MISMATCH for memory of another device or the host,
+ * MOE_ERR_UNSUPPORTED_ARCH off sm_103, MOE_ERR_CUDA if the launch fails.
+ */
+moe_status moe_selftest_wait_timeout(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Byte offsets of the forward's intermediate results inside the workspace,
  * for inspection after a forward (tests compare them with the oracle).
  * All regions are int32 unless noted; M = padded row capacity.

@@ -87,6 +87,10 @@ def test_argument_checks_before_any_device_call(L):
     assert L.moe_experts_forward_static(None, None, None, 4096, 7168, 2048, 8, 2, 0, None, None, nan, None,
                                         None) == 6
     assert L.moe_static_workspace_capacity() == 64 << 20
+    # bounded-wait self-test: null, short or misaligned workspace
+    assert L.moe_selftest_wait_timeout(None, 256, None) == 1
+    assert L.moe_selftest_wait_timeout(a, 2, None) == 1
+    assert L.moe_selftest_wait_timeout(ctypes.c_void_p(0x100002), 256, None) == 1
     # prepare (both storages): null / misaligned / unsupported shape
     for fn in (L.moe_prepare_weights, L.moe_prepare_weights_transposed):
         assert fn(0, 8, 256, 128, None, None, None, None, None, 0, None, 0, None) == 1
