@@ -65,9 +65,10 @@ namespace {
 // Prepared row -> original row, or -1 for a zero row.
 __device__ __forceinline__ int orig_row(bool is_w13, int p, int I, int H) {
   if (!is_w13) return p < H ? p : -1;
-  const int t = p / 256, r = p % 256;
-  const int q = r / 64;
-  const int j = 128 * t + 64 * (q / 2) + (r % 64);
+  static_assert(kBlockN == 4 * kGroup, "an N tile holds two gate and two up groups");
+  const int t = p / kBlockN, r = p % kBlockN;
+  const int q = r / kGroup;
+  const int j = (kBlockN / 2) * t + kGroup * (q / 2) + (r % kGroup);
   if (j >= I) return -1;
   return (q & 1) ? I + j : j;
 }
