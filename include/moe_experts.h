@@ -176,7 +176,11 @@ moe_status moe_experts_forward(const void* hidden, const int32_t* topk_idx, cons
  * `stream` at the stage boundaries: 0 before routing, 1 after routing,
  * 2 after the input quantization, 3 after GEMM1 (+SwiGLU epilogue),
  * 4 after GEMM2, 5 after the combine. `events` points to 6 entries (host
- * memory). Meant for measuring the stages; errors as moe_experts_forward.
+ * memory). Where stages share a kernel the events between them are recorded
+ * back to back: routing and quantization for T*K <= 256 (events 1 and 2),
+ * GEMM2 and the combine for FP4 weights with T*K <= 256 and T*K <= 8E
+ * (events 4 and 5). Meant for measuring the stages; errors as
+ * moe_experts_forward.
  */
 moe_status moe_experts_forward_timed(const void* hidden, const int32_t* topk_idx, const float* topk_w, int T,
                                      int H, int I, int E, int K, int fmt, const void* w13_prep,
