@@ -54,6 +54,9 @@ _SIGS = {
     "moe_experts_forward_static": (_int, [_vp, _vp, _vp, _int, _int, _int, _int, _int, _int, _vp, _vp, _f32,
                                           _vp, _vp]),
     "moe_static_workspace_capacity": (_sz, []),
+    "moe_static_get_device_status": (_int, [_vp, _c.POINTER(_c.c_uint32)]),
+    "moe_debug_forward_act_f32": (_int, [_vp, _vp, _vp, _int, _int, _int, _int, _int, _int, _vp, _vp, _f32, _vp,
+                                         _sz, _vp, _vp, _sz, _vp]),
     "moe_get_device_status": (_int, [_vp, _vp, _c.POINTER(_c.c_uint32)]),
     "moe_selftest_wait_timeout": (_int, [_vp, _c.c_size_t, _vp]),
     "moe_query_workspace_layout": (_int, [_int, _int, _int, _int, _int, _int, _c.POINTER(MoeLayout)]),
@@ -213,6 +216,33 @@ def experts_forward_static(hidden, topk_idx, topk_w, prepared, swiglu_limit=None
     return out
 
 
+def debug_forward_act_f32(hidden, topk_idx, topk_w, prepared, swiglu_limit=None, workspace=None):
+    """Test tap: the forward that also returns GEMM1's fp32 SwiGLU values,
+    [row_capacity, act_cols] in padded grouped row order (see
+    moe_debug_forward_act_f32). Returns (out, act_f32, workspace)."""
+    T, H = hidden.shape
+    K = topk_idx.shape[1]
+    p = prepared
+    lay = workspace_layout(p.fmt, T, H, p.I, p.E, K)
+    if workspace is None:
+        workspace = torch.empty(lay.total_bytes, dtype=torch.uint8, device=hidden.device)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=hidden.device)
+    act = torch.zeros(lay.row_capacity, lay.act_cols, dtype=torch.float32, device=hidden.device)
+    limit = float("nan") if swiglu_limit is None else float(swiglu_limit)
+    _check(lib().moe_debug_forward_act_f32(_ptr(hidden), _ptr(topk_idx), _ptr(topk_w), T, H, p.I, p.E, K,
+                                           FMT[p.fmt], _ptr(p.w13_prep), _ptr(p.w2_prep), limit, _ptr(workspace),
+                                           workspace.numel(), _ptr(out), _ptr(act), act.numel() * 4, _stream()),
+           "moe_debug_forward_act_f32")
+    return out, act, workspace
+
+
+def static_device_status():
+    """Synchronize and return the flags of the most recent static forward."""
+    flags = _c.c_uint32(0)
+    lib().moe_static_get_device_status(_stream(), _c.byref(flags))
+    return int(flags.value)
+
+
 def device_status(workspace):
     """Synchronize and return the forward's device flags (0 if clean)."""
     flags = _c.c_uint32(0)
@@ -237,5 +267,5 @@ def header_symbols():
 
 
 __all__ = ["lib", "MoeError", "prepare_weights", "experts_forward", "experts_forward_timed", "experts_forward_static",
-           "workspace_bytes", "workspace_layout",
+           "workspace_bytes", "workspace_layout", "debug_forward_act_f32", "static_device_status",
            "device_status", "selftest_wait_timeout", "PreparedWeights", "header_symbols", "MOE_DEV_BAD_EXPERT_ID", "MOE_DEV_TIMEOUT"]

@@ -263,7 +263,7 @@ moe_status moe_prepare_weights_transposed(int fmt, int E, int H, int I, const vo
 moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, const float* topk_w, int T, int H,
                                int I, int E, int K, int fmt, const void* w13_prep, const void* w2_prep,
                                float swiglu_limit, void* workspace, size_t workspace_bytes, void* out,
-                               void* stream, void* const* events) {
+                               void* stream, void* const* events, float* act_f32) {
   if (T < 0 || K < 1 || K > kMaxTopK) return MOE_ERR_INVALID_ARG;
   if (!shape_ok(fmt, H, I, E)) return MOE_ERR_UNSUPPORTED_SHAPE;
   WsLayout L;
@@ -345,6 +345,7 @@ moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, cons
   a1.out_sf = ws + p.asf;
   a1.out_cols = g2.Kp;
   a1.out_blocks = g2.KB;
+  a1.act_f32 = act_f32;
   a1.g = g1;
   if (launch_gemm(fmt, true, decode, ta1, tb1, a1, d.sms, st) != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;
 
@@ -388,6 +389,25 @@ moe_status moe_experts_forward_timed(const void* hidden, const int32_t* topk_idx
                                      size_t workspace_bytes, void* out, void* stream, void* const* events) {
   return forward_impl(hidden, topk_idx, topk_w, T, H, I, E, K, fmt, w13_prep, w2_prep, swiglu_limit, workspace,
                       workspace_bytes, out, stream, events);
+}
+
+moe_status moe_debug_forward_act_f32(const void* hidden, const int32_t* topk_idx, const float* topk_w, int T,
+                                     int H, int I, int E, int K, int fmt, const void* w13_prep,
+                                     const void* w2_prep, float swiglu_limit, void* workspace,
+                                     size_t workspace_bytes, void* out, float* act_f32, size_t act_f32_bytes,
+                                     void* stream) {
+  WsLayout L;
+  if (T > 0 && K >= 1 && K <= kMaxTopK && ws_layout(fmt, T, H, I, E, K, &L)) {
+    if (act_f32 == nullptr) return MOE_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(act_f32) % 32) return MOE_ERR_ALIGNMENT;
+    if (act_f32_bytes < 4ull * L.M * L.pub.act_cols) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    DevInfo d;
+    moe_status s = current_device(&d);
+    if (s != MOE_OK) return s;
+    if ((s = check_ptr(act_f32, d.id)) != MOE_OK) return s;
+  }
+  return forward_impl(hidden, topk_idx, topk_w, T, H, I, E, K, fmt, w13_prep, w2_prep, swiglu_limit, workspace,
+                      workspace_bytes, out, stream, nullptr, act_f32);
 }
 
 }  // extern "C"

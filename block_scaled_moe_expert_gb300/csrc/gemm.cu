@@ -484,6 +484,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
         tile_parity ^= 1;
         const int e = act_exponent(amax);
         const float s = exp2_neg(e);
+        if (args.act_f32 != nullptr && m < c.valid) {
+          // debug tap: the fp32 values requantized below
+          float* dst = args.act_f32 + static_cast<size_t>(row) * args.out_cols + c.nt * 128 + wg * 64;
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            st_global_v8(dst + 8 * v, __float_as_uint(ACC(8 * v)), __float_as_uint(ACC(8 * v + 1)),
+                         __float_as_uint(ACC(8 * v + 2)), __float_as_uint(ACC(8 * v + 3)),
+                         __float_as_uint(ACC(8 * v + 4)), __float_as_uint(ACC(8 * v + 5)),
+                         __float_as_uint(ACC(8 * v + 6)), __float_as_uint(ACC(8 * v + 7)));
+        }
         if (m < c.valid) {
           uint8_t* dst = args.out_q + static_cast<size_t>(row) * args.out_cols + c.nt * 128 + wg * 64;
 #pragma unroll

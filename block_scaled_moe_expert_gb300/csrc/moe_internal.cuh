@@ -147,14 +147,19 @@ struct GemmArgs {
   int K;
   __nv_bfloat16* out;         // bf16 [T][H]
   float swiglu_limit;         // > 0 and finite: clamp
+  // GEMM1 debug tap (null in every timed path): the epilogue also stores
+  // the fp32 SwiGLU values it requantizes, [M][out_cols] row-major.
+  float* act_f32;
   GemmGeom g;
 };
 
 // The whole forward on a caller-provided workspace; events (6 entries or
-// null) are recorded at the stage boundaries.
+// null) are recorded at the stage boundaries; act_f32 (null or
+// [M][act_cols] fp32) receives GEMM1's fp32 SwiGLU values.
 moe_status forward_impl(const void* hidden, const int32_t* topk_idx, const float* topk_w, int T, int H, int I,
                         int E, int K, int fmt, const void* w13_prep, const void* w2_prep, float swiglu_limit,
-                        void* workspace, size_t workspace_bytes, void* out, void* stream, void* const* events);
+                        void* workspace, size_t workspace_bytes, void* out, void* stream, void* const* events,
+                        float* act_f32 = nullptr);
 
 // decode: FP4 only; 32-row token chunks, activation tensor maps with a
 // 32-row box (tile mode: 128-row m-tiles, 128-row box); see decode_mode().

@@ -43,7 +43,12 @@
  *     moe_get_device_status;
  *   - nothing is allocated: the caller owns every buffer, including the
  *     workspace, whose size comes from moe_workspace_bytes;
- *   - a non-MOE_OK status means nothing was enqueued.
+ *   - a non-MOE_OK status means nothing was enqueued;
+ *   - element types are not checked here: every array is passed as a plain
+ *     pointer, so the caller guarantees the types the calls name (bf16
+ *     hidden and out, int32 ids, fp32 routing weights). The Python binding
+ *     refuses other dtypes (a non-bf16 hidden state raises ValueError, as
+ *     the deepgemm excerpt does) before it calls into this library.
  */
 #ifndef BSMOE_MOE_EXPERTS_H_
 #define BSMOE_MOE_EXPERTS_H_
@@ -63,7 +68,7 @@ typedef enum {
   MOE_ERR_UNSUPPORTED_SHAPE = 2,  /* dimension outside what the kernels take */
   MOE_ERR_UNSUPPORTED_ARCH = 3,   /* device is not compute capability 10.3 */
   MOE_ERR_DEVICE_MISMATCH = 4,    /* a pointer is not memory of the current device */
-  MOE_ERR_ALIGNMENT = 5,          /* a pointer is not 256-byte aligned */
+  MOE_ERR_ALIGNMENT = 5,          /* a pointer breaks its alignment rule (see Conventions) */
   MOE_ERR_WORKSPACE_TOO_SMALL = 6,
   MOE_ERR_CUDA = 7,               /* a CUDA runtime/driver call failed */
   MOE_ERR_DEVICE_FAULT = 8        /* moe_get_device_status found flags set */
@@ -205,12 +210,15 @@ moe_status moe_experts_forward_timed(const void* hidden, const int32_t* topk_idx
  *
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
- * before capturing a stream. Every call shares the one array, and its content
- * is whatever the last call left there: the forward writes every part it
- * reads before reading it, so nothing needs clearing, but calls that overlap
- * on the GPU (other streams, other host threads) race on it and must be
- * serialized by the caller. The status word of the array is not readable
- * through moe_get_device_status.
+ * before capturing a stream. The address is kept per device and looked up
+ * again when the device's context has changed (for example after
+ * cudaDeviceReset, which reloads the library's device code). Every call
+ * shares the one array, and its content is whatever the last call left
+ * there: the forward writes every part it reads before reading it, so
+ * nothing needs clearing, but calls that overlap on the GPU (other streams,
+ * other host threads) race on it and must be serialized by the caller.
+ * The flags such a call raises (MOE_DEV_BAD_EXPERT_ID, MOE_DEV_TIMEOUT) sit
+ * in the array's status word: read them with moe_static_get_device_status.
  */
 moe_status moe_experts_forward_static(const void* hidden, const int32_t* topk_idx, const float* topk_w, int T,
                                       int H, int I, int E, int K, int fmt, const void* w13_prep,
@@ -218,6 +226,17 @@ moe_status moe_experts_forward_static(const void* hidden, const int32_t* topk_id
 
 /* Bytes of the fixed device array used by moe_experts_forward_static. */
 size_t moe_static_workspace_capacity(void);
+
+/*
+ * moe_get_device_status for the fixed array of moe_experts_forward_static on
+ * the current device: synchronizes `stream`, reads the flags raised by the
+ * most recent static forward into *flags (host pointer) and clears them.
+ * Returns MOE_ERR_DEVICE_FAULT when a flag was set, MOE_OK otherwise,
+ * MOE_ERR_INVALID_ARG for a null `flags`, MOE_ERR_CUDA if a CUDA call fails.
+ * Like the forward it allocates nothing; it must not overlap a static
+ * forward running on another stream.
+ */
+moe_status moe_static_get_device_status(void* stream, uint32_t* flags);
 
 /*
  * Synchronizes `stream` and reads the status word of `workspace` into *flags
@@ -254,9 +273,6 @@ moe_status moe_selftest_wait_timeout(void* workspace, size_t workspace_bytes, vo
  *     128-row m-tiles, [1] number of 32-row chunks, [16 + e] first m-tile
  *     and [16 + E + 1 + e] first chunk of expert e (E+1 entries each), then
  *     the expert owning each m-tile, then the expert owning each chunk;
- *   tiles [16 + (E+1) + M/128]: [0] number of 128-row m-tiles, [16 + e]
- *     first m-tile of expert e (E+1 entries), then the expert owning each
- *     m-tile (GEMM work list);
  *   xq u8 [M, xq_cols] (e4m3 hidden rows in grouped order);
  *   xsf u32 (activation scale words, see below);
  *   act u8 [M, act_cols] (e4m3 SwiGLU output), asf u32 likewise;
@@ -276,6 +292,27 @@ typedef struct {
 } moe_workspace_layout;
 
 moe_status moe_query_workspace_layout(int fmt, int T, int H, int I, int E, int K, moe_workspace_layout* layout);
+
+/*
+ * Debug tap for tests: the forward of moe_experts_forward (same arguments,
+ * same kernels, same results) that also stores, from GEMM1's epilogue, the
+ * fp32 SwiGLU values it requantizes -- act = silu(gate) * up after the
+ * optional clamp -- so that the requantized bytes (workspace regions act and
+ * asf) can be checked bit for bit against the 1x128 rule applied to exactly
+ * these values. Row r of the padded grouped layout goes to
+ * act_f32[r * act_cols + j], j < act_cols (moe_query_workspace_layout;
+ * columns j >= I hold 0); padding rows are not written.
+ *   act_f32  device fp32, >= row_capacity * act_cols * 4 bytes, 32-byte
+ *            aligned (MOE_ERR_INVALID_ARG if null, MOE_ERR_ALIGNMENT,
+ *            MOE_ERR_WORKSPACE_TOO_SMALL if short).
+ * Other errors as moe_experts_forward. The extra stores make GEMM1 slower:
+ * not for timing.
+ */
+moe_status moe_debug_forward_act_f32(const void* hidden, const int32_t* topk_idx, const float* topk_w, int T,
+                                     int H, int I, int E, int K, int fmt, const void* w13_prep,
+                                     const void* w2_prep, float swiglu_limit, void* workspace,
+                                     size_t workspace_bytes, void* out, float* act_f32, size_t act_f32_bytes,
+                                     void* stream);
 
 #ifdef __cplusplus
 }

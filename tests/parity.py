@@ -49,6 +49,67 @@ def oracle_out(hidden, idx, w, weights, limit, tokens=None):
                               limit, tokens=tokens)
 
 
+def oracle_out_parallel(hidden, idx, w, weights, limit, tokens, threads=None):
+    """oracle_out for many tokens of a large workload, expert groups in threads.
+
+    The pairs of the selected tokens are split by expert into groups; each
+    group runs the oracle on its own (the other slots masked to -1, i.e.
+    skipped) and the groups' fp64 outputs are added. Only the order of the
+    fp64 additions across groups changes (relative effect ~1e-16, far below
+    the bf16 tolerances); every expert is dequantized once. numpy releases
+    the GIL in the heavy steps, so threads overlap the per-expert work.
+    """
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    ids = idx.cpu().numpy()
+    sel = ids[np.asarray(tokens)]
+    experts = np.unique(sel[(sel >= 0) & (sel < weights["E"])])
+    threads = threads or max(1, min(8, os.cpu_count() or 1))
+    groups = [experts[i::2 * threads] for i in range(min(len(experts), 2 * threads))]
+    bits = bits_of(hidden)
+    wv = w.cpu().numpy()
+
+    def run(group):
+        masked = np.where(np.isin(ids, group), ids, -1).astype(ids.dtype)
+        return OM.experts_forward(bits, masked, wv, oracle_weights(weights), limit, tokens=tokens)
+
+    out = np.zeros((len(tokens), bits.shape[1]), dtype=np.float64)
+    if not groups:
+        return out
+    with ThreadPoolExecutor(threads) as ex:
+        for part in ex.map(run, groups):
+            out += part
+    return out
+
+
+def sample_tokens(idx, E, n, seed):
+    """At least n tokens (fewer if T < n): the first and last token, one token
+    for every expert the batch touches (rarest expert first, each time the
+    earliest holder in a seeded order), then seeded random tokens."""
+    ids = idx.cpu().numpy()
+    T = ids.shape[0]
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(T)
+    pos = np.empty(T, dtype=np.int64)
+    pos[order] = np.arange(T)
+    chosen = {0, T - 1}
+    covered = set(int(e) for t in chosen for e in ids[t])
+    valid = (ids >= 0) & (ids < E)
+    counts = np.bincount(ids[valid], minlength=E)
+    for e in np.argsort(counts, kind="stable"):
+        if counts[e] == 0 or int(e) in covered:
+            continue
+        holders = np.flatnonzero((ids == e).any(axis=1))
+        t = int(holders[np.argmin(pos[holders])])
+        chosen.add(t)
+        covered.update(int(x) for x in ids[t])
+    for t in order:
+        if len(chosen) >= n:
+            break
+        chosen.add(int(t))
+    return sorted(chosen)
+
+
 def compare(gpu_bf16, ref):
     g = gpu_bf16.float().cpu().numpy().astype(np.float64)
     ref = np.asarray(ref, dtype=np.float64)
@@ -98,5 +159,5 @@ def sf_exponents(words_u32, rows, nblk):
     return (w[idx] & 0xFF) - 127
 
 
-__all__ = ["oracle_out", "compare", "assert_close", "run_cuda", "ws_region", "sf_exponents", "bits_of", "OF",
+__all__ = ["oracle_out", "oracle_out_parallel", "sample_tokens", "compare", "assert_close", "run_cuda", "ws_region", "sf_exponents", "bits_of", "OF",
            "OM", "W", "B"]

@@ -87,6 +87,15 @@ def test_argument_checks_before_any_device_call(L):
     assert L.moe_experts_forward_static(None, None, None, 4096, 7168, 2048, 8, 2, 0, None, None, nan, None,
                                         None) == 6
     assert L.moe_static_workspace_capacity() == 64 << 20
+    # ... and checks its arguments in the same order as moe_experts_forward
+    assert L.moe_experts_forward_static(None, None, None, 4, 256, 128, 8, 33, 0, None, None, nan, None, None) == 1
+    assert L.moe_experts_forward_static(None, None, None, -1, 256, 128, 8, 2, 0, None, None, nan, None, None) == 1
+    assert L.moe_experts_forward_static(None, None, None, 4, 200, 128, 8, 2, 0, None, None, nan, None, None) == 2
+    assert L.moe_experts_forward_static(None, None, None, 0, 256, 128, 8, 2, 0, None, None, nan, None, None) == 0
+    assert L.moe_static_get_device_status(None, None) == 1
+    # debug tap: null tap buffer with work to do
+    assert L.moe_debug_forward_act_f32(None, None, None, 4, 256, 128, 8, 2, 0, None, None, nan, None, 0, None,
+                                       None, 0, None) == 1
     # bounded-wait self-test: null, short or misaligned workspace
     assert L.moe_selftest_wait_timeout(None, 256, None) == 1
     assert L.moe_selftest_wait_timeout(a, 2, None) == 1

@@ -105,3 +105,42 @@ def test_reference_arm_prints_one_contract_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_gpus_flag_plan():
+    """--gpus N: runs in place inside a matching torchrun world (or alone for
+    N = 1), re-launches under torchrun with N local ranks otherwise, and
+    refuses a world size that disagrees."""
+    assert bench.launch_plan(1, {}, []) == ("run", 1)
+    assert bench.launch_plan(4, {"WORLD_SIZE": "4"}, []) == ("run", 4)
+    kind, why = bench.launch_plan(8, {"WORLD_SIZE": "2"}, [])
+    assert kind == "error" and "WORLD_SIZE=2" in why
+    assert bench.launch_plan(0, {}, [])[0] == "error"
+    kind, cmd = bench.launch_plan(2, {}, ["--gpus", "2", "--steps", "3"], port=29555)
+    assert kind == "spawn"
+    assert cmd[1:3] == ["-m", "torch.distributed.run"] and "--nproc-per-node=2" in cmd
+    assert "--master-addr=127.0.0.1" in cmd and cmd[-4:] == ["--gpus", "2", "--steps", "3"]
+
+
+def test_gpus_flag_mismatch_exits_nonzero():
+    env = dict(os.environ, WORLD_SIZE="2", RANK="0", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "4",
+                        "--workload", "tiny_fp8", "--steps", "3", "--warmup", "3"],
+                       capture_output=True, text=True, env=env, timeout=300)
+    assert r.returncode != 0 and "WORLD_SIZE=2" in r.stderr
+
+
+def test_gpus_flag_spawns_gloo_ranks():
+    """bench.py --gpus 2 without torchrun re-launches itself with 2 local
+    ranks; on the host-only reference arm they meet over gloo and rank 0
+    prints the one JSON line, with n_gpus = 2."""
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR",
+                                                            "MASTER_PORT")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--workload", "tiny_fp8", "--steps", "3", "--warmup", "3"],
+                       capture_output=True, text=True, env=env, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["config"]["parallelism"] == "replicas2"

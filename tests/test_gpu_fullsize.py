@@ -1,7 +1,9 @@
 """GPU: every workload at full size, in the launch configuration bench.py times.
 
-The oracle computes sampled tokens one by one (first, last and seeded random
-tokens); properties that hold at any size are checked on the whole output:
+The oracle computes a sample of at least 64 tokens per workload: the first and
+last token, one token for every expert the batch touches (so every touched
+expert's weights pass through the comparison), then seeded random tokens.
+Properties that hold at any size are checked on the whole output:
 routing bit-exact against the oracle's stable sort, every output finite, no
 device flag raised, and the all-skipped rows exactly zero.
 """
@@ -15,12 +17,13 @@ from tests import parity as P
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 W = P.W
-SAMPLE = {"mixtral_prefill_fp8": 4, "dsv3_decode_fp8": 6, "dsv3_prefill_fp8": 3, "gptoss_fp8xfp4": 12,
-          "dsv3_decode_fp4_T1": 1, "dsv3_decode_fp4_T8": 4, "dsv3_decode_fp4_T32": 4, "dsv3_decode_fp4_T128": 4,
-          "dsv3_decode_fp4_T512": 3, "dsv3_decode_fp4_T2048": 3}
+NAMES = ["mixtral_prefill_fp8", "dsv3_decode_fp8", "dsv3_prefill_fp8", "gptoss_fp8xfp4", "dsv3_decode_fp4_T1",
+         "dsv3_decode_fp4_T8", "dsv3_decode_fp4_T32", "dsv3_decode_fp4_T128", "dsv3_decode_fp4_T512",
+         "dsv3_decode_fp4_T2048"]
+MIN_SAMPLE = 64
 
 
-@pytest.mark.parametrize("name", list(SAMPLE), ids=str)
+@pytest.mark.parametrize("name", NAMES, ids=str)
 def test_full_size_workload(name):
     wl = W.WORKLOADS[name]
     r = P.run_cuda(wl)
@@ -40,9 +43,11 @@ def test_full_size_workload(name):
         assert (out[skipped].view(torch.int16) == 0).all()
 
     # sampled tokens against the fp64 oracle
-    rng = np.random.default_rng(wl.seed)
-    n = SAMPLE[name]
-    toks = sorted({0, wl.T - 1, *rng.choice(wl.T, size=min(n, wl.T), replace=False).tolist()})[:max(n, 1)]
-    ref = P.oracle_out(r["hidden"], r["idx"], r["w"], r["weights"], wl.swiglu_limit, tokens=toks)
+    toks = P.sample_tokens(r["idx"], wl.E, MIN_SAMPLE, wl.seed)
+    sel = r["idx"].cpu().numpy()[toks]
+    touched = set(np.unique(r["idx"].cpu().numpy()).tolist()) - {-1}
+    assert set(np.unique(sel).tolist()) - {-1} == touched
+    assert len(toks) >= min(MIN_SAMPLE, wl.T)
+    ref = P.oracle_out_parallel(r["hidden"], r["idx"], r["w"], r["weights"], wl.swiglu_limit, toks)
     m = P.assert_close(out[toks], ref, name)
-    print(name, toks, m)
+    print(name, len(toks), "tokens,", len(touched), "experts", m)

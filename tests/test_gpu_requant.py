@@ -71,3 +71,37 @@ def test_requantized_activations_match_the_oracle(wl):
         rv = OF.E4M3_TABLE[r_codes] * np.ldexp(1.0, np.repeat(r_exp, 128, axis=1)[:, :wl.I])
         scale = np.maximum(np.abs(gv), np.abs(rv))[~same]
         assert (np.abs(gv - rv)[~same] <= scale / 8 + 1e-30).all()
+
+
+@pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
+def test_requantization_is_bit_exact_on_the_epilogue_inputs(wl):
+    """The epilogue's requantization is the 1x128 rule itself: applied by the
+    oracle's quantizer to the fp32 SwiGLU values the epilogue quantized (read
+    through the debug tap; fp32 values are exact in fp64), it must give the
+    same e4m3 codes and the same exponents, bit for bit, on every valid row."""
+    dev = "cuda"
+    hidden = W.make_hidden(wl, dev)
+    idx, w = W.make_routing(wl, dev)
+    prepared = P.B.prepare_weights(W.make_weights(wl, dev))
+    out, act32, ws = P.B.debug_forward_act_f32(hidden, idx, w, prepared, wl.swiglu_limit)
+    ref_out = P.B.experts_forward(hidden, idx, w, prepared, wl.swiglu_limit)
+    torch.cuda.synchronize()
+    # the tap changes nothing else
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+
+    L = P.B.workspace_layout(wl.fmt, wl.T, wl.H, wl.I, wl.E, wl.K)
+    row_slot = P.ws_region(ws, L, "row_slot", torch.int32, L.row_capacity).cpu().numpy()
+    rows = np.flatnonzero(row_slot >= 0)
+    assert len(rows) == int((idx >= 0).sum())
+    act = P.ws_region(ws, L, "act", torch.uint8, L.row_capacity * L.act_cols)
+    act = act.view(L.row_capacity, L.act_cols).cpu().numpy()[rows]
+    words = P.ws_region(ws, L, "asf", torch.int32, L.row_capacity * L.act_blocks)
+    exps = P.sf_exponents(words, L.row_capacity, L.act_blocks)[rows]
+    a = act32.cpu().numpy().astype(np.float64)[rows]
+    assert np.isfinite(a).all()
+    assert (a[:, wl.I:] == 0).all()
+    codes, e = OF.quantize_rows_1x128(a[:, :wl.I])
+    assert np.array_equal(exps[:, :e.shape[1]], e), np.argwhere(exps[:, :e.shape[1]] != e)[:8]
+    bad = np.argwhere(act[:, :wl.I] != codes)
+    assert bad.size == 0, [(int(r), int(c), int(act[r, c]), int(codes[r, c]), float(a[r, c])) for r, c in bad[:8]]
+    assert (act[:, wl.I:] == 0).all()

@@ -272,3 +272,21 @@ def test_planted_weight_drop_is_caught():
     ref = brute_force(bits, idx, w, wt, limit)
     got = M.experts_forward(bits, idx, np.ones_like(w), wt, limit)
     assert _rel(got, ref) > 1e-3
+
+
+def test_expert_group_split_used_by_the_full_size_tests():
+    """The full-size GPU tests evaluate the oracle per group of experts in
+    threads and add the groups' outputs; that equals one oracle call up to the
+    order of fp64 additions, and the token sample covers every touched expert."""
+    from tests import parity as P
+    wl = W.Workload("split", 40, 256, 128, 16, 4, "fp4", "zipf_sigmoid", seed=77, skip_frac=0.1)
+    hidden = W.make_hidden(wl)
+    idx, w = W.make_routing(wl)
+    weights = W.make_weights(wl)
+    toks = P.sample_tokens(idx, wl.E, 12, wl.seed)
+    assert len(toks) >= 12 and toks[0] == 0 and toks[-1] == wl.T - 1
+    ids = idx.numpy()
+    assert set(np.unique(ids[toks]).tolist()) - {-1} == set(np.unique(ids).tolist()) - {-1}
+    one = P.oracle_out(hidden, idx, w, weights, None, tokens=toks)
+    split = P.oracle_out_parallel(hidden, idx, w, weights, None, toks, threads=3)
+    assert np.abs(split - one).max() <= 1e-12 * np.abs(one).max()

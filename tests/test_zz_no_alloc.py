@@ -56,3 +56,26 @@ def test_static_workspace_refuses_oversized_calls():
     st = B.lib().moe_experts_forward_static(None, None, None, wl.T, wl.H, wl.I, wl.E, wl.K, B.FMT[wl.fmt], None,
                                             None, ctypes.c_float(float("nan")), None, None)
     assert st == MOE_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_static_forward_flags_are_readable():
+    """A static forward with an out-of-range expert id treats the slot as
+    skipped and raises MOE_DEV_BAD_EXPERT_ID in the fixed array's status word,
+    which moe_static_get_device_status reads (and clears); the output equals
+    the workspace forward's on the same ids."""
+    wl = W.Workload("static_bad_id", 8, 256, 128, 8, 2, "fp8", "softmax", seed=43)
+    r = P.run_cuda(wl)
+    idx = r["idx"].clone()
+    idx[3, 1] = wl.E + 5          # out of range: skipped and flagged
+    ref = B.experts_forward(r["hidden"], idx, r["w"], r["prepared"], wl.swiglu_limit)
+    r2 = dict(r, idx=idx)
+    out = torch.full_like(r["out"], float("nan"))
+    assert _static_call(wl, r2, out) == 0
+    assert B.static_device_status() == B.MOE_DEV_BAD_EXPERT_ID
+    assert B.static_device_status() == 0     # read and cleared
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    # a clean call leaves no flag
+    assert _static_call(wl, r, out) == 0
+    assert B.static_device_status() == 0
+    assert torch.equal(out.view(torch.int16), r["out"].view(torch.int16))
