@@ -90,8 +90,8 @@ def test_requantization_is_bit_exact_on_the_epilogue_inputs(wl):
     assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
 
     L = P.B.workspace_layout(wl.fmt, wl.T, wl.H, wl.I, wl.E, wl.K)
-    row_slot = P.ws_region(ws, L, "row_slot", torch.int32, L.row_capacity).cpu().numpy()
-    rows = np.flatnonzero(row_slot >= 0)
+    inv = P.ws_region(ws, L, "inv", torch.int32, wl.T * wl.K).cpu().numpy()
+    rows = np.sort(inv[inv >= 0])
     assert len(rows) == int((idx >= 0).sum())
     act = P.ws_region(ws, L, "act", torch.uint8, L.row_capacity * L.act_cols)
     act = act.view(L.row_capacity, L.act_cols).cpu().numpy()[rows]
