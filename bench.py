@@ -158,15 +158,16 @@ def weight_bytes_per_expert(wl, which):
 
 
 def launches_per_forward(wl):
-    """Kernels one forward launches: routing + quantization (one fused kernel
-    up to 256 slots; else one routing kernel up to 8192 slots or histogram +
-    scan + scatter, then the quantization kernel), GEMM1, GEMM2, and the
-    combine (inside GEMM2 for FP4 weights with at most 8 pairs per expert
-    and at most 256 slots)."""
+    """Kernels one forward launches: one for FP4 weights with at most 8 pairs
+    per expert and at most 256 slots (the single-launch forward); otherwise
+    routing + quantization (one fused kernel up to 256 slots; else one routing
+    kernel up to 8192 slots or histogram + scan + scatter, then the
+    quantization kernel), GEMM1, GEMM2 and the combine."""
     S = wl.T * wl.K
+    if wl.fmt == "fp4" and S <= 8 * wl.E and S <= 256:
+        return 1  # the single-launch decode forward
     front = 1 if S <= 256 else (2 if S <= 8192 else 4)
-    combine = 0 if (wl.fmt == "fp4" and S <= 8 * wl.E and S <= 256) else 1
-    return front + 2 + combine
+    return front + 2 + 1
 
 
 def routing_stats(idx_cpu, E):
@@ -486,15 +487,27 @@ def run_ours(args, wl):
     # Roofline of the dominant kernel: the slower of its tensor-core time
     # (algorithmic flops / FP8 dense peak) and its HBM time (algorithmic
     # bytes: touched-expert weights + activations in and out, / bandwidth).
-    dom = max(("gemm1", "gemm2"), key=lambda k: stage_ms[k])
-    frac_1 = 2.0 / 3.0 if dom == "gemm1" else 1.0 / 3.0
-    kflops = flops * frac_1
-    wb = weight_bytes_per_expert(wl, 13 if dom == "gemm1" else 2) * touched
-    if dom == "gemm1":
-        act = pairs * (wl.H + 4 * ((wl.H + 127) // 128)) + pairs * (wl.I + 4 * ((wl.I + 127) // 128))
+    single = launches_per_forward(wl) == 1
+    if single:
+        # one kernel runs the whole forward (its time lands in the first
+        # stage; the later events are recorded back to back): its work is
+        # the forward's flops and its bytes the forward's algorithmic bytes
+        dom = "single_launch"
+        stage_ms[dom] = stage_ms["route"]
+        frac_1 = 1.0
+        kflops = flops
+        kbytes = (weight_bytes_per_expert(wl, 13) + weight_bytes_per_expert(wl, 2)) * touched \
+            + 2 * wl.T * wl.H * 2 + 8 * wl.T * wl.K
     else:
-        act = pairs * (wl.I + 4 * ((wl.I + 127) // 128)) + pairs * wl.H * 4
-    kbytes = wb + act
+        dom = max(("gemm1", "gemm2"), key=lambda k: stage_ms[k])
+        frac_1 = 2.0 / 3.0 if dom == "gemm1" else 1.0 / 3.0
+        kflops = flops * frac_1
+        wb = weight_bytes_per_expert(wl, 13 if dom == "gemm1" else 2) * touched
+        if dom == "gemm1":
+            act = pairs * (wl.H + 4 * ((wl.H + 127) // 128)) + pairs * (wl.I + 4 * ((wl.I + 127) // 128))
+        else:
+            act = pairs * (wl.I + 4 * ((wl.I + 127) // 128)) + pairs * wl.H * 4
+        kbytes = wb + act
     peak_tc_2x = 2.0 * peaks["bf16_tflops"]  # fp8 dense = 2 x bf16 dense (nominal 4.5 / 2.25 PF)
     fp8 = load_fp8_peak()
     if fp8 is not None:
@@ -517,8 +530,9 @@ def run_ours(args, wl):
         achieved = kbytes / secs / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak_hbm, "unit": "GB/s", "frac": achieved / peak_hbm,
                 "peak_source": f"{peak_src}: copy bandwidth", "frac_vs_spec_8tbs": achieved / 8000.0}
-    alg_units = (f"{frac_1:.3f} x 6*H*I*pairs flops = {kflops / 1e9:.1f} GFLOP; touched-expert weight + activation "
-                 f"bytes = {kbytes / 1e9:.3f} GB; roofline times tensor {t_tc * 1e3:.3f} ms, hbm {t_hbm * 1e3:.3f} ms")
+    alg_units = (f"{frac_1:.3f} x 6*H*I*pairs flops = {kflops / 1e9:.1f} GFLOP; touched-expert weight + "
+                 f"{'hidden, output, ids and weights' if single else 'activation'} bytes = {kbytes / 1e9:.3f} GB; "
+                 f"roofline times tensor {t_tc * 1e3:.3f} ms, hbm {t_hbm * 1e3:.3f} ms")
     traffic = measured_traffic(wl.name, dom)
     roof.update({"kernel": dom, "traffic": traffic, "traffic_unit": "bytes per launch" if traffic else None,
                  "kernel_ms": stage_ms[dom], "algorithmic": alg_units})

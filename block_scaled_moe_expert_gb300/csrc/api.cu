@@ -16,6 +16,7 @@
 
 #include "moe_internal.cuh"
 #include "ptx.cuh"
+#include "route_quant.cuh"
 
 namespace bsmoe {
 
@@ -99,19 +100,28 @@ moe_status check_ptr(const void* p, int dev) {
   return MOE_OK;
 }
 
-// Self-test of the bounded-wait path: thread 0 waits, through the helper the
-// GEMM pipeline uses, on an mbarrier phase that nothing completes. The wait
-// gives up after its bound, raises the abort flag, and the kernel reports
-// MOE_DEV_TIMEOUT the way the GEMM does, then returns.
+// Self-test of the bounded-wait paths: thread 0 waits, through the helper
+// the GEMM pipeline uses, on an mbarrier phase that nothing completes; thread
+// 32 waits, through the helper the single-launch forward's GEMM2 units use,
+// for a counter (the status word's neighbour, zeroed here) that nothing
+// increments. Each wait gives up after its bound, raises the abort flag, and
+// the kernel reports MOE_DEV_TIMEOUT the way the GEMMs do, then returns.
 __global__ void wait_timeout_selftest_kernel(uint32_t* status) {
   __shared__ __align__(8) uint64_t bar;
-  __shared__ int abort_flag;
+  __shared__ int abort_bar, abort_cnt;
   if (threadIdx.x == 0) {
-    abort_flag = 0;
+    abort_bar = 0;
     mbar_init(&bar, 1);
     fence_mbar_init();
-    const bool done = mbar_wait(&bar, 0, &abort_flag);
-    if (!done && abort_flag) atomicOr(status, MOE_DEV_TIMEOUT);
+    const bool done = mbar_wait(&bar, 0, &abort_bar);
+    if (!done && abort_bar) atomicOr(status, MOE_DEV_TIMEOUT);
+  } else if (threadIdx.x == 32) {
+    abort_cnt = 0;
+    int32_t* counter = reinterpret_cast<int32_t*>(status + 1);
+    *counter = 0;
+    __threadfence();
+    const bool done = wait_counter(counter, 1, &abort_cnt);
+    if (!done && abort_cnt) atomicOr(status, MOE_DEV_TIMEOUT);
   }
 }
 
@@ -152,6 +162,7 @@ bool ws_layout(int fmt, int T, int H, int I, int E, int K, WsLayout* out) {
     L.combine_stride = 1 + kCombineSplits * g2.NT;
     L.combine_cnt = take(4ull * static_cast<size_t>(T) * L.combine_stride);
   }
+  if (single_launch(fmt, S, E)) L.chunk_ready = take(4ull * static_cast<size_t>(M / kChunkRows));
   p.total_bytes = off;
   p.row_capacity = static_cast<int32_t>(M);
   p.row_align = kRowAlign;
@@ -263,7 +274,7 @@ moe_status moe_prepare_weights_transposed(int fmt, int E, int H, int I, const vo
 moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, const float* topk_w, int T, int H,
                                int I, int E, int K, int fmt, const void* w13_prep, const void* w2_prep,
                                float swiglu_limit, void* workspace, size_t workspace_bytes, void* out,
-                               void* stream, void* const* events, float* act_f32) {
+                               void* stream, void* const* events, float* act_f32, bool allow_single_launch) {
   if (T < 0 || K < 1 || K > kMaxTopK) return MOE_ERR_INVALID_ARG;
   if (!shape_ok(fmt, H, I, E)) return MOE_ERR_UNSUPPORTED_SHAPE;
   WsLayout L;
@@ -313,17 +324,6 @@ moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, cons
     return events == nullptr || events[i] == nullptr ||
            cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) == cudaSuccess;
   };
-  if (!mark(0)) return MOE_ERR_CUDA;
-  if (L.S <= kFusedRouteQuantSlots) {
-    // One launch for both (the quant stage then has zero length).
-    if (launch_route_quant_small(topk_idx, hidden, T, H, E, K, L, ws, out, st) != cudaSuccess || !mark(1) ||
-        !mark(2))
-      return MOE_ERR_CUDA;
-  } else {
-    if (launch_route(topk_idx, L.S, E, L, ws, st) != cudaSuccess || !mark(1)) return MOE_ERR_CUDA;
-    if (launch_quant(hidden, T, H, K, L, ws, st) != cudaSuccess || !mark(2)) return MOE_ERR_CUDA;
-  }
-
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
   a.counts = reinterpret_cast<const int32_t*>(ws + p.counts);
@@ -347,7 +347,6 @@ moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, cons
   a1.out_blocks = g2.KB;
   a1.act_f32 = act_f32;
   a1.g = g1;
-  if (launch_gemm(fmt, true, decode, ta1, tb1, a1, d.sms, st) != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;
 
   GemmArgs a2 = a;
   a2.a_sf = ws + p.asf;
@@ -363,6 +362,31 @@ moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, cons
   }
   a2.out_cols = H;
   a2.g = g2;
+
+  if (!mark(0)) return MOE_ERR_CUDA;
+  if (allow_single_launch && act_f32 == nullptr && single_launch(fmt, L.S, E)) {
+    // Small FP4 decode batches: the whole forward in one cooperative launch
+    // (the stage events after it are recorded back to back).
+    a1.chunk_ready = a2.chunk_ready = reinterpret_cast<int32_t*>(ws + L.chunk_ready);
+    a2.ready_target = g1.NT;
+    const RqArgs rq = make_rq_args(topk_idx, hidden, T, H, E, K, L, ws, out);
+    if (launch_single_decode(ta1, tb1, ta2, tb2, a1, a2, rq, d.sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+    for (int i = 1; i <= 5; ++i)
+      if (!mark(i)) return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  if (L.S <= kFusedRouteQuantSlots) {
+    // One launch for both (the quant stage then has zero length).
+    if (launch_route_quant_small(topk_idx, hidden, T, H, E, K, L, ws, out, st) != cudaSuccess || !mark(1) ||
+        !mark(2))
+      return MOE_ERR_CUDA;
+  } else {
+    if (launch_route(topk_idx, L.S, E, L, ws, st) != cudaSuccess || !mark(1)) return MOE_ERR_CUDA;
+    if (launch_quant(hidden, T, H, K, L, ws, st) != cudaSuccess || !mark(2)) return MOE_ERR_CUDA;
+  }
+
+  if (launch_gemm(fmt, true, decode, ta1, tb1, a1, d.sms, st) != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;
+
   if (launch_gemm(fmt, false, decode, ta2, tb2, a2, d.sms, st) != cudaSuccess || !mark(4)) return MOE_ERR_CUDA;
 
   // With the fused combine GEMM2 already wrote the output.
@@ -415,13 +439,13 @@ moe_status moe_debug_forward_act_f32(const void* hidden, const int32_t* topk_idx
 extern "C" {
 
 moe_status moe_selftest_wait_timeout(void* workspace, size_t workspace_bytes, void* stream) {
-  if (workspace == nullptr || workspace_bytes < sizeof(uint32_t) || reinterpret_cast<uintptr_t>(workspace) % 4)
+  if (workspace == nullptr || workspace_bytes < 2 * sizeof(uint32_t) || reinterpret_cast<uintptr_t>(workspace) % 4)
     return MOE_ERR_INVALID_ARG;
   DevInfo d;
   moe_status s = current_device(&d);
   if (s != MOE_OK) return s;
   if ((s = check_ptr(workspace, d.id)) != MOE_OK) return s;
-  wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint32_t*>(workspace));
+  wait_timeout_selftest_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint32_t*>(workspace));
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -36,11 +36,13 @@
 // byte per 32 K for both operands); the activation's 1x128 exponent is
 // replicated into four bytes, and the scale blocks are copied shared ->
 // tensor memory with tcgen05.cp before the stage's MMAs.
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
 #include "act_quant.cuh"
 #include "moe_internal.cuh"
 #include "ptx.cuh"
+#include "route_quant.cuh"
 
 namespace bsmoe {
 
@@ -169,11 +171,22 @@ __device__ __forceinline__ float ue8m0_to_float(uint32_t b) {
 // promotion can use packed fp32x2 FMAs without re-pairing registers.
 #define ACC(i) (((i) & 1) ? acc2[(i) >> 1].y : acc2[(i) >> 1].x)
 
-template <int FMT, bool GEMM1, bool DEC>
-__global__ void __launch_bounds__(kThreads, 1)
-grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                    const GemmArgs args) {
+// What one launch of the kernel body runs: GEMM1 alone, GEMM2 alone, or
+// (single-launch decode forward) routing + quantization, then GEMM1 and
+// GEMM2 units of one work list, GEMM2 units waiting on their chunk's GEMM1
+// units.
+enum : int { kG1 = 0, kG2 = 1, kBoth = 2 };
+
+// The kernel body. Side 1 (ta1, tb1, a1) is the only GEMM for KIND kG1 /
+// kG2; for kBoth work units [0, U1) are GEMM1's and [U1, total) GEMM2's
+// (side 2), U1 and total taken from the routing tables after the grid-wide
+// barrier that ends the routing + quantization phase (rq).
+template <int FMT, int KIND, bool DEC>
+__device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensorMap* tb1, const GemmArgs& a1,
+                                          const CUtensorMap* ta2, const CUtensorMap* tb2, const GemmArgs& a2,
+                                          const RqArgs* rq) {
   static_assert(!DEC || FMT == MOE_W_FP4, "decode mode is built for FP4 weights");
+  static_assert(KIND != kBoth || DEC, "the single-launch forward runs the decode mode");
   using Smem = SmemT<DEC>;
   constexpr int kStages = Pipe<DEC>::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -181,11 +194,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
   // __shared__ array itself so the compiler keeps shared-space addressing.
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const GemmGeom g = args.g;
-  const int KB = g.KB, NT = g.NT;
   volatile int* abort_flag = &sm.abort_flag;
-  auto tile_of = [&](int idx) {
-    return decode_tile<DEC>(idx, args.E, args.M, NT, args.tiles, args.counts, args.padded_offsets);
+  int U1 = 0;  // kBoth: number of GEMM1 units
+  // Per work unit: which GEMM (side 1 or 2), its arguments and index.
+  auto on_side1 = [&](int idx) { return KIND != kBoth || idx < U1; };
+  auto is_gemm1 = [&](int idx) { return KIND == kG1 || (KIND == kBoth && idx < U1); };
+  auto tile_at = [&](int idx) {
+    const bool s1 = on_side1(idx);
+    const GemmArgs& A = s1 ? a1 : a2;
+    return decode_tile<DEC>(s1 ? idx : idx - U1, A.E, A.M, A.g.NT, A.tiles, A.counts, A.padded_offsets);
   };
 
   if (tid == 0) {
@@ -224,51 +241,109 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
   // every GEMM1 CTA has passed its own wait, i.e. before the routing kernel
   // has finished.
   int pre_unit = -1, pre_n = 0;
-  if constexpr (DEC && !GEMM1) {
-    if (tid == 0 && static_cast<int>(blockIdx.x) < __ldg(args.tiles + 1) * NT) {
-      const TileCoord c = tile_of(blockIdx.x);
-      pre_unit = blockIdx.x;
-      pre_n = min(kStages, KB);
-      const int wrow = c.e * g.Np + c.nt * kBlockN;
-      for (int s = 0; s < pre_n; ++s) {
-        mbar_arrive_expect_tx(&sm.full[s], kStageBytes);
-        tma_load_2d(sm.b[s], &tmap_b, &sm.full[s], s * kBlockK, wrow);
-        bulk_load(sm.sfb[s], args.w_scale + ((static_cast<size_t>(c.e) * NT + c.nt) * KB + s) * kSfbBytes, kSfbBytes,
-                  &sm.full[s]);
+  int total_tiles = 0;
+  if constexpr (KIND == kBoth) {
+    // Routing + quantization of the small batch (every CTA routes the whole
+    // batch in shared memory, borrowing the weight ring; CTA 0 writes the
+    // routing arrays and zeroes the chunk counters; each CTA quantizes its
+    // tokens), then a grid-wide barrier: every unit below may read any of it.
+    RqSmem<kThreads / 32>& rs = *reinterpret_cast<RqSmem<kThreads / 32>*>(&sm.b[0][0]);
+    route_small_in_smem<kThreads / 32>(rs, *rq);
+    if (blockIdx.x == 0) write_routing<kThreads / 32>(rs, *rq);
+    quantize_tokens<kThreads / 32>(rs, *rq, blockIdx.x, gridDim.x);
+    const int nchunks = rs.chs[rq->E];
+    // the generic-proxy writes above (global: routing arrays, counters;
+    // shared: the borrowed ring) are ordered before the TMA traffic below
+    __threadfence();
+    fence_proxy_async_global();
+    fence_proxy_async_smem();
+    cooperative_groups::this_grid().sync();
+    fence_proxy_async_global();
+    U1 = nchunks * a1.g.NT;
+    total_tiles = U1 + nchunks * a2.g.NT;
+  } else {
+    if constexpr (DEC && KIND == kG2) {
+      const GemmGeom& g = a1.g;
+      if (tid == 0 && static_cast<int>(blockIdx.x) < __ldg(a1.tiles + 1) * g.NT) {
+        const TileCoord c = tile_at(blockIdx.x);
+        pre_unit = blockIdx.x;
+        pre_n = min(kStages, g.KB);
+        const int wrow = c.e * g.Np + c.nt * kBlockN;
+        for (int s = 0; s < pre_n; ++s) {
+          mbar_arrive_expect_tx(&sm.full[s], kStageBytes);
+          tma_load_2d(sm.b[s], tb1, &sm.full[s], s * kBlockK, wrow);
+          bulk_load(sm.sfb[s], a1.w_scale + ((static_cast<size_t>(c.e) * g.NT + c.nt) * g.KB + s) * kSfbBytes,
+                    kSfbBytes, &sm.full[s]);
+        }
       }
     }
+    // Everything above overlaps the previous kernel's tail; the tile list and
+    // the activations are written by the kernels before this one.
+    pdl_wait();
+    pdl_launch_dependents();
+    total_tiles = __ldg(a1.tiles + (DEC ? 1 : 0)) * a1.g.NT;
   }
-  // Everything above overlaps the previous kernel's tail; the tile list and
-  // the activations are written by the kernels before this one.
-  pdl_wait();
-  pdl_launch_dependents();
-  const int total_tiles = __ldg(args.tiles + (DEC ? 1 : 0)) * NT;
 
   if (warp < kEpiWarp0) {
    regs_dec<56>();
    if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch_desc(&tmap_a);
-      tma_prefetch_desc(&tmap_b);
+      tma_prefetch_desc(ta1);
+      tma_prefetch_desc(tb1);
+      if constexpr (KIND == kBoth) {
+        tma_prefetch_desc(ta2);
+        tma_prefetch_desc(tb2);
+      }
       int stage = 0;
       uint32_t phase = 0;
       for (int idx = blockIdx.x; idx < total_tiles && !*abort_flag; idx += gridDim.x) {
-        const TileCoord c = tile_of(idx);
-        const int wrow = c.e * g.Np + c.nt * kBlockN;
-        for (int kb = 0; kb < KB; ++kb) {
+        const bool s1 = on_side1(idx);
+        const GemmArgs& A = s1 ? a1 : a2;
+        const CUtensorMap* TA = s1 ? ta1 : ta2;
+        const CUtensorMap* TB = s1 ? tb1 : tb2;
+        const int KB = A.g.KB, NT = A.g.NT;
+        const TileCoord c = tile_at(idx);
+        const int wrow = c.e * A.g.Np + c.nt * kBlockN;
+        int kb0 = 0;
+        if (KIND == kBoth && !s1) {
+          // GEMM2 unit of the single-launch forward: the weight side of the
+          // first stages now; the activation side once every GEMM1 unit of
+          // this chunk has stored its rows (bounded wait on the counter).
+          const int npre = min(kStages, KB);
+          const int st0 = stage;
+          bool ok = true;
+          for (int kb = 0; kb < npre; ++kb) {
+            if (!mbar_wait(&sm.empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
+            mbar_arrive_expect_tx(&sm.full[stage], kStageBytes);
+            tma_load_2d(sm.b[stage], TB, &sm.full[stage], kb * kBlockK, wrow);
+            bulk_load(sm.sfb[stage], A.w_scale + ((static_cast<size_t>(c.e) * NT + c.nt) * KB + kb) * kSfbBytes,
+                      kSfbBytes, &sm.full[stage]);
+            if (++stage == kStages) { stage = 0; phase ^= 1; }
+          }
+          if (!ok || !wait_counter(A.chunk_ready + c.row0 / kChunkRows, A.ready_target, abort_flag)) break;
+          fence_proxy_async_global();
+          for (int kb = 0; kb < npre; ++kb) {
+            const int s = (st0 + kb) % kStages;
+            tma_load_2d(sm.a_stage(s), TA, &sm.full[s], kb * kBlockK, c.row0);
+            bulk_load(sm.sfa[s], A.a_sf + (static_cast<size_t>(c.row0 / kBlockM) * KB + kb) * kSfaBytes, kSfaBytes,
+                      &sm.full[s]);
+          }
+          kb0 = npre;
+        }
+        for (int kb = kb0; kb < KB; ++kb) {
           if (!mbar_wait(&sm.empty[stage], phase ^ 1, abort_flag)) break;
           // weights already in flight from before the dependency wait
           const bool pre = idx == pre_unit && kb < pre_n;
           if (!pre) mbar_arrive_expect_tx(&sm.full[stage], kStageBytes);
-          tma_load_2d(sm.a_stage(stage), &tmap_a, &sm.full[stage], kb * kBlockK, c.row0);
-          if (!pre) tma_load_2d(sm.b[stage], &tmap_b, &sm.full[stage], kb * kBlockK, wrow);
+          tma_load_2d(sm.a_stage(stage), TA, &sm.full[stage], kb * kBlockK, c.row0);
+          if (!pre) tma_load_2d(sm.b[stage], TB, &sm.full[stage], kb * kBlockK, wrow);
           if constexpr (FMT == MOE_W_FP4) {
-            bulk_load(sm.sfa[stage], args.a_sf + (static_cast<size_t>(c.row0 / kBlockM) * KB + kb) * kSfaBytes,
+            bulk_load(sm.sfa[stage], A.a_sf + (static_cast<size_t>(c.row0 / kBlockM) * KB + kb) * kSfaBytes,
                       kSfaBytes, &sm.full[stage]);
             if (!pre)
               bulk_load(sm.sfb[stage],
-                        args.w_scale + ((static_cast<size_t>(c.e) * NT + c.nt) * KB + kb) * kSfbBytes, kSfbBytes,
+                        A.w_scale + ((static_cast<size_t>(c.e) * NT + c.nt) * KB + kb) * kSfbBytes, kSfbBytes,
                         &sm.full[stage]);
           }
           if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -285,6 +360,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
       int buf = 0;
       uint32_t bphase = 0;
       for (int idx = blockIdx.x; idx < total_tiles && !*abort_flag; idx += gridDim.x) {
+        const int KB = (on_side1(idx) ? a1 : a2).g.KB;
         if constexpr (FMT == MOE_W_FP8) {
           constexpr uint32_t idesc = idesc_f8f6f4(0, 0, kBlockM, kBlockN);
           for (int kb = 0; kb < KB; ++kb) {
@@ -311,7 +387,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
           // its 128-row block's image; the MMA reads A rows 0-31 (the chunk)
           // from the first column.
           int q = 0;
-          if constexpr (DEC) q = (tile_of(idx).row0 % kBlockM) / kChunkRows;
+          if constexpr (DEC) q = (tile_at(idx).row0 % kBlockM) / kChunkRows;
           for (int kb = 0; kb < KB; ++kb) {
             bool okf = mbar_wait(&sm.full[stage], phase, abort_flag);
             if constexpr (DEC) okf = __all_sync(0xffffffffu, okf);
@@ -359,8 +435,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
     if (lane == 0) {
       int slot = 0;
       uint32_t sphase = 0;
+      const GemmArgs& args = a1;
+      const int KB = args.g.KB, NT = args.g.NT;
       for (int idx = blockIdx.x; idx < total_tiles && !*abort_flag; idx += gridDim.x) {
-        const TileCoord c = tile_of(idx);
+        const TileCoord c = tile_at(idx);
         for (int kb0 = 0; kb0 < KB; kb0 += kScaleGroup) {
           const int n = min(kScaleGroup, KB - kb0);
           if (!mbar_wait(&sm.sempty[slot], sphase ^ 1, abort_flag)) break;
@@ -386,10 +464,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
     int sslot = 0;
     uint32_t ssphase = 0;
     int tile_parity = 0;
-    const float limit = args.swiglu_limit;
+    const float limit = a1.swiglu_limit;
     const bool clamp = limit > 0.f && limit < INFINITY;
     for (int idx = blockIdx.x; idx < total_tiles && !*abort_flag; idx += gridDim.x) {
-      const TileCoord c = tile_of(idx);
+      const bool GEMM1 = is_gemm1(idx);
+      const GemmArgs& args = on_side1(idx) ? a1 : a2;
+      const int KB = args.g.KB;
+      const TileCoord c = tile_at(idx);
       float2 acc2[64];
       bool ok = true;
       if constexpr (FMT == MOE_W_FP8) {
@@ -459,7 +540,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
         }
       }
       const int row = c.row0 + m;
-      if constexpr (GEMM1) {
+      if (GEMM1) {
         // ACC(0..63) = gate, ACC(64..127) = up of intermediate columns
         // j = 128 nt + 64 wg + i.
         float amax = 0.f;
@@ -509,6 +590,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
           if (wg == 0)
             reinterpret_cast<uint32_t*>(args.out_sf)[sf_word_index(row, c.nt, args.out_blocks)] =
                 static_cast<uint32_t>(e + 127) * 0x01010101u;
+        }
+        if constexpr (KIND == kBoth) {
+          // Release this unit's rows to the GEMM2 units of the chunk: every
+          // thread's stores, a fence, the epilogue barrier, then one count.
+          __threadfence();
+          fence_proxy_async_global();
+          epi_barrier_any(false);
+          if (tid == kEpiWarp0 * 32) atomicAdd(args.chunk_ready + c.row0 / kChunkRows, 1);
         }
       } else {
         if (!ok) break;
@@ -601,7 +690,25 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tbase, kTmemCols);
-  if (tid == 0 && sm.abort_flag) atomicOr(args.status, MOE_DEV_TIMEOUT);
+  if (tid == 0 && sm.abort_flag) atomicOr(a1.status, MOE_DEV_TIMEOUT);
+}
+
+template <int FMT, bool GEMM1, bool DEC>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                    const __grid_constant__ GemmArgs args) {
+  gemm_body<FMT, GEMM1 ? kG1 : kG2, DEC>(&tmap_a, &tmap_b, args, &tmap_a, &tmap_b, args, nullptr);
+}
+
+// The single-launch decode forward (FP4 weights, T * K <= 256): routing,
+// quantization, GEMM1 + SwiGLU + requantization, GEMM2 + routing weight +
+// the top-k combine, in one cooperative launch of one CTA per SM.
+__global__ void __launch_bounds__(kThreads, 1)
+single_launch_decode_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constant__ CUtensorMap tb1,
+                            const __grid_constant__ CUtensorMap ta2, const __grid_constant__ CUtensorMap tb2,
+                            const __grid_constant__ GemmArgs a1, const __grid_constant__ GemmArgs a2,
+                            const __grid_constant__ RqArgs rq) {
+  gemm_body<MOE_W_FP4, kBoth, true>(&ta1, &tb1, a1, &ta2, &tb2, a2, &rq);
 }
 
 template <int FMT, bool GEMM1, bool DEC>
@@ -614,7 +721,38 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const GemmA
   return launch_kernel(true, kern, num_sms, kThreads, smem, st, ta, tb, args);
 }
 
+static_assert(sizeof(RqSmem<kThreads / 32>) <= sizeof(SmemT<true>::b),
+              "the routing + quantization phase borrows the weight ring");
+
 }  // namespace
+
+cudaError_t launch_single_decode(const CUtensorMap& ta1, const CUtensorMap& tb1, const CUtensorMap& ta2,
+                                 const CUtensorMap& tb2, const GemmArgs& a1, const GemmArgs& a2, const RqArgs& rq,
+                                 int num_sms, cudaStream_t st) {
+  auto kern = single_launch_decode_kernel;
+  const int smem = static_cast<int>(sizeof(SmemT<true>)) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+  // Cooperative: every CTA is resident at once (the grid-wide barrier after
+  // routing and the GEMM2 units' waits on GEMM1 units rely on it). The first
+  // kernel of the forward: an ordinary (not programmatic) dependency on what
+  // the caller queued before.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, ta1, tb1, ta2, tb2, a1, a2, rq);
+}
 
 cudaError_t launch_gemm(int fmt, bool is_gemm1, bool decode, const CUtensorMap& ta, const CUtensorMap& tb,
                         const GemmArgs& args, int num_sms, cudaStream_t st) {

@@ -59,6 +59,9 @@ struct WsLayout {
   // arrival counter per (GEMM2 n tile, column half).
   size_t combine_cnt;
   int combine_stride;
+  // Single-launch decode forward only (0 otherwise): int32 [M / 32], per
+  // 32-row chunk the number of GEMM1 units that have stored their rows.
+  size_t chunk_ready;
 };
 
 // Number of routing chunks for S slots (0: the single-CTA kernel is used).
@@ -115,6 +118,11 @@ cudaError_t launch_route_quant_small(const int32_t* topk_idx, const void* hidden
 inline bool fused_combine(int fmt, long long S, int E) {
   return decode_mode(fmt, S, E) && S <= kFusedRouteQuantSlots;
 }
+// The whole forward as one cooperative launch (routing + quantization, then
+// the GEMM1 and GEMM2 units of one work list, GEMM2 units waiting on device
+// counters for their chunk's GEMM1 units; the combine in GEMM2's epilogue):
+// the same batches as the fused combine.
+inline bool single_launch(int fmt, long long S, int E) { return fused_combine(fmt, S, E); }
 cudaError_t launch_combine(const float* y, const int32_t* inv, int T, int H, int K, void* out, cudaStream_t st);
 // transposed: the weights are stored [E][K][N] (N contiguous) instead of [E][N][K].
 cudaError_t launch_prepare(int fmt, bool transposed, int E, int H, int I, const void* w13, const void* w13s,
@@ -150,20 +158,31 @@ struct GemmArgs {
   // GEMM1 debug tap (null in every timed path): the epilogue also stores
   // the fp32 SwiGLU values it requantizes, [M][out_cols] row-major.
   float* act_f32;
+  // Single-launch decode forward: per 32-row chunk, the number of GEMM1
+  // units that have stored their rows; a GEMM2 unit waits for ready_target.
+  int32_t* chunk_ready;
+  int ready_target;
   GemmGeom g;
 };
 
 // The whole forward on a caller-provided workspace; events (6 entries or
 // null) are recorded at the stage boundaries; act_f32 (null or
-// [M][act_cols] fp32) receives GEMM1's fp32 SwiGLU values.
+// [M][act_cols] fp32) receives GEMM1's fp32 SwiGLU values and selects the
+// multi-kernel sequence (the single-launch forward has no tap).
 moe_status forward_impl(const void* hidden, const int32_t* topk_idx, const float* topk_w, int T, int H, int I,
                         int E, int K, int fmt, const void* w13_prep, const void* w2_prep, float swiglu_limit,
                         void* workspace, size_t workspace_bytes, void* out, void* stream, void* const* events,
-                        float* act_f32 = nullptr);
+                        float* act_f32 = nullptr, bool allow_single_launch = true);
 
 // decode: FP4 only; 32-row token chunks, activation tensor maps with a
 // 32-row box (tile mode: 128-row m-tiles, 128-row box); see decode_mode().
 cudaError_t launch_gemm(int fmt, bool is_gemm1, bool decode, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                         const GemmArgs& args, int num_sms, cudaStream_t st);
+
+struct RqArgs;
+// The single-launch decode forward: one cooperative launch of num_sms CTAs.
+cudaError_t launch_single_decode(const CUtensorMap& ta1, const CUtensorMap& tb1, const CUtensorMap& ta2,
+                                 const CUtensorMap& tb2, const GemmArgs& a1, const GemmArgs& a2, const RqArgs& rq,
+                                 int num_sms, cudaStream_t st);
 
 }  // namespace bsmoe

@@ -63,6 +63,30 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Bounded wait until *p >= target (acquire at GPU scope), for counters that
+// other CTAs of the same grid increment. Returns false if the CTA aborted or
+// the wait ran out of time (then sets the abort flag).
+__device__ __forceinline__ bool wait_counter(const int32_t* p, int target, volatile int* abort_flag) {
+  const long long t0 = clock64();
+  while (true) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= target) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort_flag = 1;
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
+
+// Orders this thread's generic-proxy accesses of global memory with async-
+// proxy (TMA, bulk copy) accesses on the other side of a synchronization.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Same as mbar_wait but polls without suspending the thread: for the short
 // handshakes on the critical path (TMEM buffers), where a suspended waiter
 // would wake up late.

@@ -247,13 +247,16 @@ moe_status moe_static_get_device_status(void* stream, uint32_t* flags);
 moe_status moe_get_device_status(void* workspace, void* stream, uint32_t* flags);
 
 /*
- * Self-test of the failure path of the pipeline waits. Enqueues on `stream`
- * one CTA whose thread waits, through the same bounded mbarrier wait the
- * GEMMs use, on a phase that nothing completes. After its bound (2e9 SM
- * clock cycles, about one second) the wait gives up and the kernel ORs
- * MOE_DEV_TIMEOUT into the status word of `workspace` (its first 4 bytes,
- * device memory of the current device, 4-byte aligned) and returns; the
- * context stays usable. Read the result with moe_get_device_status.
+ * Self-test of the failure path of the bounded waits. Enqueues on `stream`
+ * one CTA in which one thread waits, through the same bounded mbarrier wait
+ * the GEMMs use, on a phase that nothing completes, and another waits,
+ * through the same bounded counter wait the single-launch forward's GEMM2
+ * units use, for the second word of `workspace` (set to 0 first) to reach 1,
+ * which nothing does. After their bound (2e9 SM clock cycles, about one
+ * second) the waits give up and the kernel ORs MOE_DEV_TIMEOUT into the
+ * status word of `workspace` (its first 4 bytes; 8 bytes of device memory of
+ * the current device, 4-byte aligned) and returns; the context stays usable.
+ * Read the result with moe_get_device_status.
  * Returns MOE_ERR_INVALID_ARG for a null, short or misaligned workspace,
  * MOE_ERR_DEVICE_MISMATCH for memory of another device or the host,
  * MOE_ERR_UNSUPPORTED_ARCH off sm_103, MOE_ERR_CUDA if the launch fails.
@@ -295,7 +298,10 @@ moe_status moe_query_workspace_layout(int fmt, int T, int H, int I, int E, int K
 
 /*
  * Debug tap for tests: the forward of moe_experts_forward (same arguments,
- * same kernels, same results) that also stores, from GEMM1's epilogue, the
+ * same results) run as the multi-kernel sequence (routing, quantization,
+ * GEMM1, GEMM2, combine as separate launches, also for the small FP4 decode
+ * batches that moe_experts_forward runs as one launch), which also stores,
+ * from GEMM1's epilogue, the
  * fp32 SwiGLU values it requantizes -- act = silu(gate) * up after the
  * optional clamp -- so that the requantized bytes (workspace regions act and
  * asf) can be checked bit for bit against the 1x128 rule applied to exactly

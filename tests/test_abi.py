@@ -99,6 +99,7 @@ def test_argument_checks_before_any_device_call(L):
     # bounded-wait self-test: null, short or misaligned workspace
     assert L.moe_selftest_wait_timeout(None, 256, None) == 1
     assert L.moe_selftest_wait_timeout(a, 2, None) == 1
+    assert L.moe_selftest_wait_timeout(a, 4, None) == 1  # needs the status word and a counter
     assert L.moe_selftest_wait_timeout(ctypes.c_void_p(0x100002), 256, None) == 1
     # prepare (both storages): null / misaligned / unsupported shape
     for fn in (L.moe_prepare_weights, L.moe_prepare_weights_transposed):

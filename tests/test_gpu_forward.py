@@ -214,3 +214,31 @@ def test_fp4_small_decode_batches_match_larger_batches(T, K, E):
     w2 = torch.cat([w, torch.rand(extra, K, generator=g, device="cuda")])
     out = P.B.experts_forward(hid, idx2, w2, r["prepared"])
     assert torch.equal(out[:T].view(torch.int16), r["out"].view(torch.int16))
+
+
+@pytest.mark.parametrize("T,H,I,E,K,skip", [(1, 7168, 2048, 256, 8, 0.0), (8, 1024, 512, 64, 8, 0.05),
+                                            (32, 512, 384, 256, 8, 0.0), (40, 320, 192, 32, 4, 0.3),
+                                            (100, 256, 128, 64, 2, 0.0)])
+def test_single_launch_forward_matches_the_kernel_sequence(T, H, I, E, K, skip):
+    """Small FP4 decode batches (at most 8 pairs per expert, at most 256
+    slots) run the whole forward as one cooperative launch: routing and
+    quantization, then one work list of GEMM1 and GEMM2 units in which every
+    GEMM2 unit waits on device counters for its chunk's GEMM1 units, the
+    combine in GEMM2's epilogue. The same inputs through the multi-kernel
+    sequence (the debug entry point runs it) give the same bits, twice in a
+    row, and both match the oracle."""
+    wl = W.Workload(f"single_T{T}", T, H, I, E, K, "fp4", "zipf_sigmoid", seed=60 + T, skip_frac=skip,
+                    swiglu_limit=7.0 if T == 8 else None)
+    assert wl.S <= 256 and wl.S <= 8 * wl.E
+    r = P.run_cuda(wl)
+    assert P.B.device_status(r["ws"]) == 0
+    for _ in range(2):
+        out = P.B.experts_forward(r["hidden"], r["idx"], r["w"], r["prepared"], wl.swiglu_limit, workspace=r["ws"])
+        seq, _, ws2 = P.B.debug_forward_act_f32(r["hidden"], r["idx"], r["w"], r["prepared"], wl.swiglu_limit)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), r["out"].view(torch.int16))
+        assert torch.equal(seq.view(torch.int16), r["out"].view(torch.int16))
+        assert P.B.device_status(r["ws"]) == 0 and P.B.device_status(ws2) == 0
+    toks = list(range(min(T, 24)))
+    ref = P.oracle_out_parallel(r["hidden"], r["idx"], r["w"], r["weights"], wl.swiglu_limit, toks)
+    P.assert_close(r["out"][toks], ref, wl.name)
