@@ -77,10 +77,15 @@ struct Pipe {
   static constexpr uint32_t kARegion = kStages * kAStride + (kTileABytes - kAStride);
 };
 
+constexpr uint32_t kYBoxBytes = 32 * 16 * 4;
+
 template <bool DEC>
 struct __align__(1024) SmemT {
   uint8_t b[Pipe<DEC>::kStages][kTileBBytes];
   uint8_t a[Pipe<DEC>::kARegion];  // stage s at s * kAStride (1024-byte aligned)
+  // GEMM2 in tile mode: per epilogue warp, a 32-row x 16-column fp32 box
+  // through which its row stores are transposed (tile mode only).
+  uint8_t ystage[DEC ? 16 : kEpiThreads / 32 * kYBoxBytes];
   uint8_t sfa[Pipe<DEC>::kStages][kSfaBytes];
   uint8_t sfb[Pipe<DEC>::kStages][kSfbBytes];
   uint64_t full[Pipe<DEC>::kStages];
@@ -526,6 +531,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
           tc_fence_after();
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
+            // a warp whose 32 rows are all padding (light experts' last
+            // tiles) reads nothing; it still takes part in the hand-off
+            if (quarter * 32 >= c.valid) break;
             uint32_t r[32];
             tmem_ld_32x32b_x32(tbase + lane_base + wg * 128 + q * 32, r);
             tmem_wait_ld();
@@ -603,7 +611,40 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
         if (!ok) break;
         bool last = false;
         int t_last = 0;
-        if (m < c.valid) {
+        if (!DEC) {
+          // Tile mode: the warp's 32 rows leave in 16-column boxes transposed
+          // through shared memory, so that each store instruction writes 64
+          // contiguous bytes of 8 rows instead of 32 bytes of 32 rows (a
+          // lane per row): the per-SM store rate of the fp32 rows bounds this
+          // phase. The lane of row r writes 16-byte piece p of its box row at
+          // r * 64 + (p ^ ((r / 2) % 4)) * 16, conflict-free on both sides.
+          float wgt = 0.f;
+          if (m < c.valid) wgt = __ldg(args.topk_w + __ldg(args.row_slot + row));
+          const float2 w2 = make_float2(wgt, wgt);
+          const int col0 = c.nt * kBlockN + wg * 128;
+          const uint32_t stg = smem_u32(sm.ystage) + (warp - kEpiWarp0) * kYBoxBytes;
+          const int rr = lane >> 2, pp = lane & 3;  // read-back: row rr + 8 i, piece pp
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (col0 + 16 * j < args.H) {  // warp-uniform (an if: a break here spills)
+#pragma unroll
+              for (int p = 0; p < 4; ++p) {
+                const float2 lo = __fmul2_rn(acc2[8 * j + 2 * p], w2), hi = __fmul2_rn(acc2[8 * j + 2 * p + 1], w2);
+                st_shared_v4(stg + lane * 64 + ((p ^ ((lane >> 1) & 3)) << 4), lo.x, lo.y, hi.x, hi.y);
+              }
+              __syncwarp();
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int r = 8 * i + rr;
+                const float4 v = ld_shared_v4(stg + r * 64 + ((pp ^ ((r >> 1) & 3)) << 4));
+                if (quarter * 32 + r < c.valid)
+                  *reinterpret_cast<float4*>(args.out_y + static_cast<size_t>(c.row0 + quarter * 32 + r) * args.H +
+                                             col0 + 16 * j + 4 * pp) = v;
+              }
+              __syncwarp();
+            }
+          }
+        } else if (m < c.valid) {
           const int slot = __ldg(args.row_slot + row);
           const float wgt = __ldg(args.topk_w + slot);
           const int col0 = c.nt * kBlockN + wg * 128;
