@@ -45,7 +45,7 @@ DEFAULT_WORKLOAD = "dsv3_prefill_fp8"
 FP8_PEAK_RECORD = os.path.join(ROOT, "profiles", "fp8_peak.json")
 STAGES = ["route", "quant", "gemm1", "gemm2", "combine"]
 L2_FLUSH_BYTES = 256 << 20
-CPU_SAMPLE_TOKENS = {"mixtral_prefill_fp8": 24, "dsv3_prefill_fp8": 3, "dsv3_decode_fp8": 3, "gptoss_fp8xfp4": 24}
+CPU_SAMPLE_TOKENS = {"mixtral_prefill_fp8": 24, "dsv3_prefill_fp8": 12, "dsv3_decode_fp8": 6, "gptoss_fp8xfp4": 24}
 
 
 def load_peaks():
@@ -159,15 +159,17 @@ def weight_bytes_per_expert(wl, which):
 
 def launches_per_forward(wl):
     """Kernels one forward launches: one for FP4 weights with at most 8 pairs
-    per expert and at most 256 slots (the single-launch forward); otherwise
+    per expert and at most 32 slots (the single-launch forward); otherwise
     routing + quantization (one fused kernel up to 256 slots; else one routing
     kernel up to 8192 slots or histogram + scan + scatter, then the
-    quantization kernel), GEMM1, GEMM2 and the combine."""
+    quantization kernel), GEMM1, GEMM2, and the combine (inside GEMM2 for FP4
+    weights with at most 8 pairs per expert and at most 256 slots)."""
     S = wl.T * wl.K
-    if wl.fmt == "fp4" and S <= 8 * wl.E and S <= 256:
+    if wl.fmt == "fp4" and S <= 8 * wl.E and S <= 32:
         return 1  # the single-launch decode forward
     front = 1 if S <= 256 else (2 if S <= 8192 else 4)
-    return front + 2 + 1
+    combine = 0 if (wl.fmt == "fp4" and S <= 8 * wl.E and S <= 256) else 1
+    return front + 2 + combine
 
 
 def routing_stats(idx_cpu, E):
@@ -637,6 +639,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=0)
     ap.add_argument("--tokens", type=int, default=0, help="override T (smaller profiling cases)")
+    ap.add_argument("--experts", type=int, default=0, help="override E (smaller profiling cases)")
     args = ap.parse_args()
     if args.calibrate_fp8:
         calibrate_fp8(args)
@@ -652,6 +655,8 @@ def main():
     wl = W.WORKLOADS[args.workload]
     if args.tokens:
         wl = W.scaled(wl, T=args.tokens)
+    if args.experts:
+        wl = W.scaled(wl, E=args.experts)
     if args.impl == "reference":
         run_reference(args, wl)
     else:

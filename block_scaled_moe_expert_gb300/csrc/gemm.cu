@@ -315,6 +315,11 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
           // GEMM2 unit of the single-launch forward: the weight side of the
           // first stages now; the activation side once every GEMM1 unit of
           // this chunk has stored its rows (bounded wait on the counter).
+          // The counter is first read (relaxed) before the weight copies are
+          // issued, so that an already complete chunk costs no round trip.
+          const int32_t* ready = A.chunk_ready + c.row0 / kChunkRows;
+          int seen;
+          asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(seen) : "l"(ready) : "memory");
           const int npre = min(kStages, KB);
           const int st0 = stage;
           bool ok = true;
@@ -326,7 +331,12 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
                       kSfbBytes, &sm.full[stage]);
             if (++stage == kStages) { stage = 0; phase ^= 1; }
           }
-          if (!ok || !wait_counter(A.chunk_ready + c.row0 / kChunkRows, A.ready_target, abort_flag)) break;
+          if (!ok) break;
+          if (seen >= A.ready_target) {
+            asm volatile("fence.acq_rel.gpu;" ::: "memory");  // the relaxed read + fence acquire
+          } else if (!wait_counter(ready, A.ready_target, abort_flag)) {
+            break;
+          }
           fence_proxy_async_global();
           for (int kb = 0; kb < npre; ++kb) {
             const int s = (st0 + kb) % kStages;

@@ -120,9 +120,15 @@ inline bool fused_combine(int fmt, long long S, int E) {
 }
 // The whole forward as one cooperative launch (routing + quantization, then
 // the GEMM1 and GEMM2 units of one work list, GEMM2 units waiting on device
-// counters for their chunk's GEMM1 units; the combine in GEMM2's epilogue):
-// the same batches as the fused combine.
-inline bool single_launch(int fmt, long long S, int E) { return fused_combine(fmt, S, E); }
+// counters for their chunk's GEMM1 units; the combine in GEMM2's epilogue),
+// for fused-combine batches of at most kSingleLaunchSlots slots. Measured at
+// the DeepSeek-V3 shape (FP4, K = 8), one launch against the kernel
+// sequence: T=1 0.0652 vs 0.0706 ms, T=2 0.0942 vs 0.0971, T=4 0.1372 vs
+// 0.1380, T=8 0.2161 vs 0.2088, T=16 0.3549 vs 0.3263.
+constexpr int kSingleLaunchSlots = 32;
+inline bool single_launch(int fmt, long long S, int E) {
+  return fused_combine(fmt, S, E) && S <= kSingleLaunchSlots;
+}
 cudaError_t launch_combine(const float* y, const int32_t* inv, int T, int H, int K, void* out, cudaStream_t st);
 // transposed: the weights are stored [E][K][N] (N contiguous) instead of [E][N][K].
 cudaError_t launch_prepare(int fmt, bool transposed, int E, int H, int I, const void* w13, const void* w13s,

@@ -169,6 +169,12 @@ moe_status moe_prepare_weights_transposed(int fmt, int E, int H, int I, const vo
  * Ids outside [-1, E) are treated as skipped and set MOE_DEV_BAD_EXPERT_ID.
  * Asynchronous; the workspace must not be used by another call until this
  * one has finished on `stream`.
+ *
+ * Launches: routing + quantization, GEMM1, GEMM2 and the combine; for FP4
+ * weights with T*K <= 8E (the weight-streaming decode batches) and
+ * T*K <= 32 the whole forward is one cooperative launch of one CTA per SM
+ * (GEMM2 work units wait on device counters for the GEMM1 units of their
+ * rows), which needs every SM of the device free for the launch.
  */
 moe_status moe_experts_forward(const void* hidden, const int32_t* topk_idx, const float* topk_w, int T, int H,
                                int I, int E, int K, int fmt, const void* w13_prep, const void* w2_prep,
@@ -184,8 +190,9 @@ moe_status moe_experts_forward(const void* hidden, const int32_t* topk_idx, cons
  * memory). Where stages share a kernel the events between them are recorded
  * back to back: routing and quantization for T*K <= 256 (events 1 and 2),
  * GEMM2 and the combine for FP4 weights with T*K <= 256 and T*K <= 8E
- * (events 4 and 5). Meant for measuring the stages; errors as
- * moe_experts_forward.
+ * (events 4 and 5), and every stage for FP4 weights with T*K <= 32 and
+ * T*K <= 8E, which run as one launch (events 1 to 5 after it). Meant for
+ * measuring the stages; errors as moe_experts_forward.
  */
 moe_status moe_experts_forward_timed(const void* hidden, const int32_t* topk_idx, const float* topk_w, int T,
                                      int H, int I, int E, int K, int fmt, const void* w13_prep,

@@ -216,11 +216,11 @@ def test_fp4_small_decode_batches_match_larger_batches(T, K, E):
     assert torch.equal(out[:T].view(torch.int16), r["out"].view(torch.int16))
 
 
-@pytest.mark.parametrize("T,H,I,E,K,skip", [(1, 7168, 2048, 256, 8, 0.0), (8, 1024, 512, 64, 8, 0.05),
-                                            (32, 512, 384, 256, 8, 0.0), (40, 320, 192, 32, 4, 0.3),
-                                            (100, 256, 128, 64, 2, 0.0)])
+@pytest.mark.parametrize("T,H,I,E,K,skip", [(1, 7168, 2048, 256, 8, 0.0), (4, 1024, 512, 64, 8, 0.05),
+                                            (2, 512, 384, 256, 8, 0.0), (8, 320, 192, 32, 4, 0.3),
+                                            (16, 256, 128, 64, 2, 0.0), (32, 256, 128, 8, 1, 0.0)])
 def test_single_launch_forward_matches_the_kernel_sequence(T, H, I, E, K, skip):
-    """Small FP4 decode batches (at most 8 pairs per expert, at most 256
+    """Small FP4 decode batches (at most 8 pairs per expert, at most 32
     slots) run the whole forward as one cooperative launch: routing and
     quantization, then one work list of GEMM1 and GEMM2 units in which every
     GEMM2 unit waits on device counters for its chunk's GEMM1 units, the
@@ -229,7 +229,7 @@ def test_single_launch_forward_matches_the_kernel_sequence(T, H, I, E, K, skip):
     row, and both match the oracle."""
     wl = W.Workload(f"single_T{T}", T, H, I, E, K, "fp4", "zipf_sigmoid", seed=60 + T, skip_frac=skip,
                     swiglu_limit=7.0 if T == 8 else None)
-    assert wl.S <= 256 and wl.S <= 8 * wl.E
+    assert wl.S <= 32 and wl.S <= 8 * wl.E
     r = P.run_cuda(wl)
     assert P.B.device_status(r["ws"]) == 0
     for _ in range(2):
