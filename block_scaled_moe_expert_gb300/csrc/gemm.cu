@@ -302,6 +302,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
       }
       int stage = 0;
       uint32_t phase = 0;
+      int pf_idx = -1, pf_seen = 0;  // single launch: next GEMM2 unit's counter, read ahead
       for (int idx = blockIdx.x; idx < total_tiles && !*abort_flag; idx += gridDim.x) {
         const bool s1 = on_side1(idx);
         const GemmArgs& A = s1 ? a1 : a2;
@@ -312,41 +313,62 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
         const int wrow = c.e * A.g.Np + c.nt * kBlockN;
         int kb0 = 0;
         if (KIND == kBoth && !s1) {
-          // GEMM2 unit of the single-launch forward: the weight side of the
-          // first stages now; the activation side once every GEMM1 unit of
-          // this chunk has stored its rows (bounded wait on the counter).
-          // The counter is first read (relaxed) before the weight copies are
-          // issued, so that an already complete chunk costs no round trip.
+          // GEMM2 unit of the single-launch forward. Its chunk's counter was
+          // read (relaxed) while the previous unit was being issued; if the
+          // chunk was complete then, an acquire fence makes its rows visible
+          // and the unit takes the ordinary path. Otherwise the weight side
+          // of the first stages goes out now and the activation side once
+          // every GEMM1 unit of the chunk has stored its rows (bounded wait).
           const int32_t* ready = A.chunk_ready + c.row0 / kChunkRows;
-          int seen;
-          asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(seen) : "l"(ready) : "memory");
-          const int npre = min(kStages, KB);
-          const int st0 = stage;
-          bool ok = true;
-          for (int kb = 0; kb < npre; ++kb) {
-            if (!mbar_wait(&sm.empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
-            mbar_arrive_expect_tx(&sm.full[stage], kStageBytes);
-            tma_load_2d(sm.b[stage], TB, &sm.full[stage], kb * kBlockK, wrow);
-            bulk_load(sm.sfb[stage], A.w_scale + ((static_cast<size_t>(c.e) * NT + c.nt) * KB + kb) * kSfbBytes,
-                      kSfbBytes, &sm.full[stage]);
-            if (++stage == kStages) { stage = 0; phase ^= 1; }
+          int seen = 0;
+          if (pf_idx == idx) {
+            seen = pf_seen;
+          } else {
+            asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(seen) : "l"(ready) : "memory");
           }
-          if (!ok) break;
           if (seen >= A.ready_target) {
             asm volatile("fence.acq_rel.gpu;" ::: "memory");  // the relaxed read + fence acquire
-          } else if (!wait_counter(ready, A.ready_target, abort_flag)) {
-            break;
+            fence_proxy_async_global();
+          } else {
+            const int npre = min(kStages, KB);
+            const int st0 = stage;
+            bool ok = true;
+            for (int kb = 0; kb < npre; ++kb) {
+              if (!mbar_wait(&sm.empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
+              mbar_arrive_expect_tx(&sm.full[stage], kStageBytes);
+              tma_load_2d(sm.b[stage], TB, &sm.full[stage], kb * kBlockK, wrow);
+              bulk_load(sm.sfb[stage], A.w_scale + ((static_cast<size_t>(c.e) * NT + c.nt) * KB + kb) * kSfbBytes,
+                        kSfbBytes, &sm.full[stage]);
+              if (++stage == kStages) { stage = 0; phase ^= 1; }
+            }
+            if (!ok || !wait_counter(ready, A.ready_target, abort_flag)) break;
+            fence_proxy_async_global();
+            for (int kb = 0; kb < npre; ++kb) {
+              const int s = (st0 + kb) % kStages;
+              tma_load_2d(sm.a_stage(s), TA, &sm.full[s], kb * kBlockK, c.row0);
+              bulk_load(sm.sfa[s], A.a_sf + (static_cast<size_t>(c.row0 / kBlockM) * KB + kb) * kSfaBytes,
+                        kSfaBytes, &sm.full[s]);
+            }
+            kb0 = npre;
           }
-          fence_proxy_async_global();
-          for (int kb = 0; kb < npre; ++kb) {
-            const int s = (st0 + kb) % kStages;
-            tma_load_2d(sm.a_stage(s), TA, &sm.full[s], kb * kBlockK, c.row0);
-            bulk_load(sm.sfa[s], A.a_sf + (static_cast<size_t>(c.row0 / kBlockM) * KB + kb) * kSfaBytes, kSfaBytes,
-                      &sm.full[s]);
-          }
-          kb0 = npre;
         }
         for (int kb = kb0; kb < KB; ++kb) {
+          if constexpr (KIND == kBoth) {
+            // read the next unit's chunk counter ahead (its value is used at
+            // that unit's start); placed a few stages in, so that the table
+            // loads it needs do not delay this unit's first copies
+            if (kb == kb0 + 2 || (kb == kb0 && KB - kb0 <= 2)) {
+              const int nidx = idx + static_cast<int>(gridDim.x);
+              if (nidx >= U1 && nidx < total_tiles) {
+                const TileCoord nc = tile_at(nidx);
+                asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];"
+                             : "=r"(pf_seen)
+                             : "l"(a2.chunk_ready + nc.row0 / kChunkRows)
+                             : "memory");
+                pf_idx = nidx;
+              }
+            }
+          }
           if (!mbar_wait(&sm.empty[stage], phase ^ 1, abort_flag)) break;
           // weights already in flight from before the dependency wait
           const bool pre = idx == pre_unit && kb < pre_n;
