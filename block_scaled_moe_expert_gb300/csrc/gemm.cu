@@ -396,7 +396,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
       uint32_t phase = 0;
       int buf = 0;
       uint32_t bphase = 0;
-      for (int idx = blockIdx.x; idx < total_tiles && !*abort_flag; idx += gridDim.x) {
+      // (decode mode: the whole warp walks the stages, so it leaves together)
+      for (int idx = blockIdx.x; idx < total_tiles && !(DEC ? __any_sync(0xffffffffu, *abort_flag != 0) : *abort_flag);
+           idx += gridDim.x) {
         const int KB = (on_side1(idx) ? a1 : a2).g.KB;
         if constexpr (FMT == MOE_W_FP8) {
           constexpr uint32_t idesc = idesc_f8f6f4(0, 0, kBlockM, kBlockN);
@@ -503,7 +505,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
     int tile_parity = 0;
     const float limit = a1.swiglu_limit;
     const bool clamp = limit > 0.f && limit < INFINITY;
-    for (int idx = blockIdx.x; idx < total_tiles && !*abort_flag; idx += gridDim.x) {
+    // (no abort test in the loop condition: a thread that saw the flag
+    // early would leave while the others wait at the epilogue barrier; after
+    // an abort every wait fails and the reducing barrier stops them together)
+    for (int idx = blockIdx.x; idx < total_tiles; idx += gridDim.x) {
       const bool GEMM1 = is_gemm1(idx);
       const GemmArgs& args = on_side1(idx) ? a1 : a2;
       const int KB = args.g.KB;
@@ -558,7 +563,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
           if (buf == 0) bphase ^= 1;
         }
       } else {
-        if (!mbar_wait(&sm.tfull[0], bphase, abort_flag)) ok = false;
+        // warp-uniform: the drain below is made of warp-collective loads
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.tfull[0], bphase, abort_flag));
         if (ok) {
           tc_fence_after();
 #pragma unroll
@@ -640,7 +646,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
           if (tid == kEpiWarp0 * 32) atomicAdd(args.chunk_ready + c.row0 / kChunkRows, 1);
         }
       } else {
-        if (!ok) break;
+        // warp-uniform: the stores and the fused combine below use warp
+        // barriers and shuffles
+        if (!__all_sync(0xffffffffu, ok)) break;
         bool last = false;
         int t_last = 0;
         if (!DEC) {
