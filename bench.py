@@ -321,8 +321,11 @@ def _reference_line(args, wl, ws):
             pairs.append(routing_stats(ids[t:t + 1], wl.E)[0])
     total = sum(times)
     flops = 6.0 * wl.H * wl.I * sum(pairs)
-    # the same config keys as the GPU arm, from the host-generated full batch
-    full_pairs, full_touched = routing_stats(W.make_routing(wl)[0].numpy(), wl.E)
+    # the same config keys as the GPU arm: its routing is drawn on the device
+    # (the device generator's stream differs from the host's), so the full
+    # batch's routing is drawn there when a device exists (not timed)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    full_pairs, full_touched = routing_stats(W.make_routing(wl, dev)[0].cpu().numpy(), wl.E)
     value = flops / total / 1e12
     cores = len(os.sched_getaffinity(0))
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
