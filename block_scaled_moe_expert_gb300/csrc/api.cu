@@ -157,6 +157,7 @@ bool ws_layout(int fmt, int T, int H, int I, int E, int K, WsLayout* out) {
   p.act = take(static_cast<size_t>(M) * g2.Kp);
   p.asf = take(4ull * M * g2.KB);
   p.y = take(4ull * M * H);
+  L.row_w = take(4ull * M);
   L.route_scratch = take(4ull * (static_cast<size_t>(route_chunks(static_cast<int>(S))) + 1) * (E + 1));
   if (fused_combine(fmt, S, E)) {
     L.combine_stride = 1 + kCombineSplits * g2.NT;
@@ -330,7 +331,7 @@ moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, cons
   a.padded_offsets = reinterpret_cast<const int32_t*>(ws + p.padded_offsets);
   a.tiles = reinterpret_cast<const int32_t*>(ws + p.tiles);
   a.row_slot = reinterpret_cast<const int32_t*>(ws + p.row_slot);
-  a.topk_w = topk_w;
+  a.row_w = reinterpret_cast<const float*>(ws + L.row_w);
   a.status = reinterpret_cast<uint32_t*>(ws + p.status);
   a.E = E;
   a.I = I;
@@ -369,7 +370,7 @@ moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, cons
     // (the stage events after it are recorded back to back).
     a1.chunk_ready = a2.chunk_ready = reinterpret_cast<int32_t*>(ws + L.chunk_ready);
     a2.ready_target = g1.NT;
-    const RqArgs rq = make_rq_args(topk_idx, hidden, T, H, E, K, L, ws, out);
+    const RqArgs rq = make_rq_args(topk_idx, hidden, topk_w, T, H, E, K, L, ws, out);
     if (launch_single_decode(ta1, tb1, ta2, tb2, a1, a2, rq, d.sms, st) != cudaSuccess) return MOE_ERR_CUDA;
     for (int i = 1; i <= 5; ++i)
       if (!mark(i)) return MOE_ERR_CUDA;
@@ -377,12 +378,12 @@ moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, cons
   }
   if (L.S <= kFusedRouteQuantSlots) {
     // One launch for both (the quant stage then has zero length).
-    if (launch_route_quant_small(topk_idx, hidden, T, H, E, K, L, ws, out, st) != cudaSuccess || !mark(1) ||
+    if (launch_route_quant_small(topk_idx, hidden, topk_w, T, H, E, K, L, ws, out, st) != cudaSuccess || !mark(1) ||
         !mark(2))
       return MOE_ERR_CUDA;
   } else {
     if (launch_route(topk_idx, L.S, E, L, ws, st) != cudaSuccess || !mark(1)) return MOE_ERR_CUDA;
-    if (launch_quant(hidden, T, H, K, L, ws, st) != cudaSuccess || !mark(2)) return MOE_ERR_CUDA;
+    if (launch_quant(hidden, topk_w, T, H, K, L, ws, st) != cudaSuccess || !mark(2)) return MOE_ERR_CUDA;
   }
 
   if (launch_gemm(fmt, true, decode, ta1, tb1, a1, d.sms, st) != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;

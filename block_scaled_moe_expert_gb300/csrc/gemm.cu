@@ -659,7 +659,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
           // phase. The lane of row r writes 16-byte piece p of its box row at
           // r * 64 + (p ^ ((r / 2) % 4)) * 16, conflict-free on both sides.
           float wgt = 0.f;
-          if (m < c.valid) wgt = __ldg(args.topk_w + __ldg(args.row_slot + row));
+          if (m < c.valid) wgt = __ldg(args.row_w + row);
           const float2 w2 = make_float2(wgt, wgt);
           const int col0 = c.nt * kBlockN + wg * 128;
           const uint32_t stg = smem_u32(sm.ystage) + (warp - kEpiWarp0) * kYBoxBytes;
@@ -685,8 +685,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
             }
           }
         } else if (m < c.valid) {
-          const int slot = __ldg(args.row_slot + row);
-          const float wgt = __ldg(args.topk_w + slot);
+          const float wgt = __ldg(args.row_w + row);
+          const int slot = (DEC && args.combine_cnt != nullptr) ? __ldg(args.row_slot + row) : 0;
           const int col0 = c.nt * kBlockN + wg * 128;
           float* dst = args.out_y + static_cast<size_t>(row) * args.H + col0;
 #pragma unroll

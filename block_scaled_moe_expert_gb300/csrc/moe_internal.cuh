@@ -62,6 +62,10 @@ struct WsLayout {
   // Single-launch decode forward only (0 otherwise): int32 [M / 32], per
   // 32-row chunk the number of GEMM1 units that have stored their rows.
   size_t chunk_ready;
+  // fp32 [M]: the routing weight of the slot in each padded row, written by
+  // the quantization next to the row's codes (padding rows are not written
+  // and never read), so that GEMM2's epilogue needs one load per row.
+  size_t row_w;
 };
 
 // Number of routing chunks for S slots (0: the single-CTA kernel is used).
@@ -103,14 +107,15 @@ cudaError_t launch_kernel(bool dependent, void (*kern)(KArgs...), dim3 grid, dim
 
 // ---------------------------------------------------------------- launches
 cudaError_t launch_route(const int32_t* topk_idx, int S, int E, const WsLayout& L, uint8_t* ws, cudaStream_t st);
-cudaError_t launch_quant(const void* hidden, int T, int H, int K, const WsLayout& L, uint8_t* ws, cudaStream_t st);
+cudaError_t launch_quant(const void* hidden, const float* topk_w, int T, int H, int K, const WsLayout& L, uint8_t* ws,
+                         cudaStream_t st);
 // Routing + quantization in one launch, for S = T * K <= kFusedRouteQuantSlots.
 // With the fused combine (below) it also sets that up: per-token valid-slot
 // counts, zeroed arrival counters, and the +0 output rows of tokens whose
 // slots are all skipped.
 constexpr int kFusedRouteQuantSlots = 256;
-cudaError_t launch_route_quant_small(const int32_t* topk_idx, const void* hidden, int T, int H, int E, int K,
-                                     const WsLayout& L, uint8_t* ws, void* out, cudaStream_t st);
+cudaError_t launch_route_quant_small(const int32_t* topk_idx, const void* hidden, const float* topk_w, int T, int H,
+                                     int E, int K, const WsLayout& L, uint8_t* ws, void* out, cudaStream_t st);
 // The top-k combine fused into GEMM2's epilogue: decode mode with the fused
 // routing + quantization front end. At larger decode batches the separate
 // combine kernel is faster (the epilogue's combines then hold up the
@@ -142,7 +147,7 @@ struct GemmArgs {
   const int32_t* padded_offsets;
   const int32_t* tiles;
   const int32_t* row_slot;
-  const float* topk_w;
+  const float* row_w;         // GEMM2: routing weight per padded row
   uint32_t* status;
   // outputs
   uint8_t* out_q;             // GEMM1: e4m3 act [M][act_cols]

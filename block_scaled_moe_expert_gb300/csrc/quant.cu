@@ -20,8 +20,9 @@ constexpr int kQuantWarps = 8;
 // One CTA per token: gathers the token's valid slots from inv (in ascending
 // k) and quantizes the row into each of their padded rows.
 __global__ void __launch_bounds__(kQuantWarps * 32)
-quant_permute_kernel(const __nv_bfloat16* __restrict__ hidden, int H, int K, int Kp,
-                     const int32_t* __restrict__ inv, uint8_t* __restrict__ xq, uint32_t* __restrict__ xsf) {
+quant_permute_kernel(const __nv_bfloat16* __restrict__ hidden, const float* __restrict__ topk_w, int H, int K, int Kp,
+                     const int32_t* __restrict__ inv, uint8_t* __restrict__ xq, uint32_t* __restrict__ xsf,
+                     float* __restrict__ row_w) {
   const int t = blockIdx.x;
   __shared__ int rows[kMaxTopK];
   __shared__ int nrows;
@@ -33,7 +34,10 @@ quant_permute_kernel(const __nv_bfloat16* __restrict__ hidden, int H, int K, int
     int n = 0;
     for (int k = 0; k < K; ++k) {
       const int r = __ldg(inv + static_cast<size_t>(t) * K + k);
-      if (r >= 0) rows[n++] = r;
+      if (r >= 0) {
+        rows[n++] = r;
+        row_w[r] = __ldg(topk_w + static_cast<size_t>(t) * K + k);
+      }
     }
     nrows = n;
   }
@@ -56,18 +60,22 @@ __global__ void __launch_bounds__(kQuantWarps * 32) route_quant_small_kernel(con
 
 }  // namespace
 
-cudaError_t launch_quant(const void* hidden, int T, int H, int K, const WsLayout& L, uint8_t* ws, cudaStream_t st) {
+cudaError_t launch_quant(const void* hidden, const float* topk_w, int T, int H, int K, const WsLayout& L, uint8_t* ws,
+                         cudaStream_t st) {
   const moe_workspace_layout& p = L.pub;
   return launch_kernel(true, quant_permute_kernel, T, kQuantWarps * 32, 0, st,
-                       reinterpret_cast<const __nv_bfloat16*>(hidden), H, K, p.xq_cols,
-                       reinterpret_cast<const int32_t*>(ws + p.inv), ws + p.xq, reinterpret_cast<uint32_t*>(ws + p.xsf));
+                       reinterpret_cast<const __nv_bfloat16*>(hidden), topk_w, H, K, p.xq_cols,
+                       reinterpret_cast<const int32_t*>(ws + p.inv), ws + p.xq, reinterpret_cast<uint32_t*>(ws + p.xsf),
+                       reinterpret_cast<float*>(ws + L.row_w));
 }
 
-RqArgs make_rq_args(const int32_t* topk_idx, const void* hidden, int T, int H, int E, int K, const WsLayout& L,
-                    uint8_t* ws, void* out) {
+RqArgs make_rq_args(const int32_t* topk_idx, const void* hidden, const float* topk_w, int T, int H, int E, int K,
+                    const WsLayout& L, uint8_t* ws, void* out) {
   const moe_workspace_layout& p = L.pub;
   RqArgs a;
   a.idx = topk_idx;
+  a.topk_w = topk_w;
+  a.row_w = reinterpret_cast<float*>(ws + L.row_w);
   a.hidden = reinterpret_cast<const __nv_bfloat16*>(hidden);
   a.T = T;
   a.S = T * K;
@@ -94,12 +102,13 @@ RqArgs make_rq_args(const int32_t* topk_idx, const void* hidden, int T, int H, i
   return a;
 }
 
-cudaError_t launch_route_quant_small(const int32_t* topk_idx, const void* hidden, int T, int H, int E, int K,
+cudaError_t launch_route_quant_small(const int32_t* topk_idx, const void* hidden, const float* topk_w, int T, int H,
+                                     int E, int K,
                                      const WsLayout& L, uint8_t* ws, void* out, cudaStream_t st) {
   // The first kernel of the forward is an ordinary launch: it follows
   // whatever the caller queued on the stream.
   return launch_kernel(false, route_quant_small_kernel, T, kQuantWarps * 32, 0, st,
-                       make_rq_args(topk_idx, hidden, T, H, E, K, L, ws, out));
+                       make_rq_args(topk_idx, hidden, topk_w, T, H, E, K, L, ws, out));
 }
 
 }  // namespace bsmoe

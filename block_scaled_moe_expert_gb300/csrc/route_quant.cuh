@@ -137,6 +137,8 @@ __device__ __forceinline__ int warp_incl_scan(int x) {
 struct RqArgs {
   const int32_t* idx;          // [T, K] expert ids
   const __nv_bfloat16* hidden; // [T, H]
+  const float* topk_w;         // [T, K] routing weights
+  float* row_w;                // [M] routing weight per padded row (written for valid rows)
   int T, S, E, K, H, Kp, M;
   int32_t* counts;
   int32_t* offsets;
@@ -309,7 +311,11 @@ __device__ __forceinline__ void quantize_tokens(RqSmem<kNW>& sm, const RqArgs& a
       int n = 0;
       for (int k = 0; k < a.K; ++k) {
         const int s = t * a.K + k;
-        if (sm.key[s] < a.E) sm.rows[n++] = sm.pad[sm.key[s]] + sm.rank[s];
+        if (sm.key[s] < a.E) {
+          const int r = sm.pad[sm.key[s]] + sm.rank[s];
+          sm.rows[n++] = r;
+          a.row_w[r] = __ldg(a.topk_w + s);
+        }
       }
       sm.nrows = n;
     }
@@ -324,7 +330,7 @@ __device__ __forceinline__ void quantize_tokens(RqSmem<kNW>& sm, const RqArgs& a
 }
 
 // Host: the arguments for a forward on workspace `ws` with layout L.
-RqArgs make_rq_args(const int32_t* topk_idx, const void* hidden, int T, int H, int E, int K, const WsLayout& L,
-                    uint8_t* ws, void* out);
+RqArgs make_rq_args(const int32_t* topk_idx, const void* hidden, const float* topk_w, int T, int H, int E, int K,
+                    const WsLayout& L, uint8_t* ws, void* out);
 
 }  // namespace bsmoe
