@@ -255,7 +255,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
     RqSmem<kThreads / 32>& rs = *reinterpret_cast<RqSmem<kThreads / 32>*>(&sm.b[0][0]);
     route_small_in_smem<kThreads / 32>(rs, *rq);
     if (blockIdx.x == 0) write_routing<kThreads / 32>(rs, *rq);
-    quantize_tokens<kThreads / 32>(rs, *rq, blockIdx.x, gridDim.x);
+    quantize_tokens<kThreads / 32, true>(rs, *rq, blockIdx.x, gridDim.x);
     const int nchunks = rs.chs[rq->E];
     // the generic-proxy writes above (global: routing arrays, counters;
     // shared: the borrowed ring) are ordered before the TMA traffic below

@@ -43,7 +43,7 @@ quant_permute_kernel(const __nv_bfloat16* __restrict__ hidden, const float* __re
   }
   __syncthreads();
   if (nrows == 0) return;
-  quantize_token<kQuantWarps>(hidden + static_cast<size_t>(t) * H, H, Kp, rows, nrows, xq, xsf, qrow, qsf);
+  quantize_token<kQuantWarps, false>(hidden + static_cast<size_t>(t) * H, H, Kp, rows, nrows, xq, xsf, qrow, qsf);
 }
 
 // ---------------------------------------------------------------------------
@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(kQuantWarps * 32) route_quant_small_kernel(con
   pdl_launch_dependents();
   route_small_in_smem<kQuantWarps>(sm, a);
   if (blockIdx.x == 0) write_routing<kQuantWarps>(sm, a);
-  quantize_tokens<kQuantWarps>(sm, a, blockIdx.x, gridDim.x);
+  quantize_tokens<kQuantWarps, false>(sm, a, blockIdx.x, gridDim.x);
 }
 
 }  // namespace

@@ -43,6 +43,11 @@ __device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t 
 __device__ __forceinline__ void bulk_store_commit_and_wait() {
   asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group 0;" ::: "memory");
 }
+// Only until the copies have read their shared-memory source; the global
+// writes finish on their own and are complete when the grid is.
+__device__ __forceinline__ void bulk_store_commit_and_wait_read() {
+  asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 
 // Quantizes one token row and copies its bytes to the n padded rows listed
 // in `rows`, with all kNW warps of the CTA. A warp covers 256 columns (two
@@ -54,7 +59,10 @@ __device__ __forceinline__ void bulk_store_commit_and_wait() {
 // writing them with per-lane stores, eight rows of a token took 3-4 µs of
 // store issue alone.
 constexpr int kLoadBatch = 4;
-template <int kNW>
+// kComplete: wait for the rows' global writes to complete (they are read in
+// the same grid after a grid-wide barrier); otherwise only until the copies
+// have read shared memory (a later kernel reads the rows).
+template <int kNW, bool kComplete>
 __device__ __forceinline__ void quantize_token(const __nv_bfloat16* __restrict__ xr, int H, int Kp,
                                                const int* rows, int n, uint8_t* __restrict__ xq,
                                                uint32_t* __restrict__ xsf, uint8_t* qrow, uint32_t* qsf) {
@@ -105,8 +113,14 @@ __device__ __forceinline__ void quantize_token(const __nv_bfloat16* __restrict__
     const int i = j / nblk, b = j - i * nblk;
     xsf[sf_word_index(rows[i], b, nblk)] = qsf[b];
   }
-  // the copies read shared memory until they complete
-  if (threadIdx.x == 0) bulk_store_commit_and_wait();
+  // the copies read shared memory until then
+  if (threadIdx.x == 0) {
+    if constexpr (kComplete) {
+      bulk_store_commit_and_wait();
+    } else {
+      bulk_store_commit_and_wait_read();
+    }
+  }
   __syncthreads();
 }
 
@@ -304,7 +318,7 @@ __device__ __forceinline__ void write_routing(RqSmem<kNW>& sm, const RqArgs& a) 
 
 // Tokens t0, t0 + stride, ... : the valid slots' padded rows (ascending k),
 // the fused-combine setup, and the quantization into those rows.
-template <int kNW>
+template <int kNW, bool kComplete>
 __device__ __forceinline__ void quantize_tokens(RqSmem<kNW>& sm, const RqArgs& a, int t0, int stride) {
   for (int t = t0; t < a.T; t += stride) {
     if (threadIdx.x == 0) {
@@ -323,7 +337,7 @@ __device__ __forceinline__ void quantize_tokens(RqSmem<kNW>& sm, const RqArgs& a
     const int n = sm.nrows;
     if (a.comb_cnt != nullptr) setup_combine(t, n, a.comb_cnt, a.comb_stride, a.out, a.H);
     if (n > 0)
-      quantize_token<kNW>(a.hidden + static_cast<size_t>(t) * a.H, a.H, a.Kp, sm.rows, n, a.xq, a.xsf, sm.qrow,
+      quantize_token<kNW, kComplete>(a.hidden + static_cast<size_t>(t) * a.H, a.H, a.Kp, sm.rows, n, a.xq, a.xsf, sm.qrow,
                           sm.qsf);
     __syncthreads();  // rows / nrows are rewritten for the next token
   }
