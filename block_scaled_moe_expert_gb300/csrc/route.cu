@@ -239,12 +239,22 @@ route_scan_kernel(int E, int M, int G, int32_t* __restrict__ chunk_hist, int32_t
   if (tid == 0) *status = 0u;
   int cnt = 0;
   if (tid <= E) {  // exclusive prefix over chunks, in place
+    // eight chunks' counts are loaded before any of them is overwritten, so
+    // the loads of a batch are in flight together
+    constexpr int kBatch = 8;
     int run = 0;
-    for (int g = 0; g < G; ++g) {
-      int32_t* c = chunk_hist + static_cast<size_t>(g) * (E + 1) + tid;
-      const int v = *c;
-      *c = run;
-      run += v;
+    for (int g0 = 0; g0 < G; g0 += kBatch) {
+      int v[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j)
+        v[j] = (g0 + j < G) ? chunk_hist[static_cast<size_t>(g0 + j) * (E + 1) + tid] : 0;
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        if (g0 + j < G) {
+          chunk_hist[static_cast<size_t>(g0 + j) * (E + 1) + tid] = run;
+          run += v[j];
+        }
+      }
     }
     cnt = run;
   }
