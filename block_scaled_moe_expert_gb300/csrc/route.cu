@@ -205,7 +205,7 @@ route_kernel(const int32_t* __restrict__ idx, int S, int E, int M, int32_t* __re
 // chunk places its slots with the same per-warp stable ranking as above.
 // The placement is identical to the single-CTA kernel's.
 
-constexpr int kChunk = 2048;
+constexpr int kChunk = 1024;
 constexpr int kChunkWarps = 8;
 
 __global__ void __launch_bounds__(kChunkWarps * 32)

@@ -67,7 +67,7 @@ CASES = [
     # separate routing and quantization kernels
     P.W.scaled(P.W.WORKLOADS["dsv3_decode_fp8"], T=32, H=256, I=128),
     P.W.scaled(P.W.WORKLOADS["dsv3_decode_fp8"], T=33, H=256, I=128),
-    # more than 8192 slots: the multi-CTA routing path (5 and 17 chunks)
+    # more than 8192 slots: the multi-CTA routing path (10 and 34 chunks of 1024 slots)
     P.W.scaled(P.W.WORKLOADS["dsv3_decode_fp8"], T=1250, H=256, I=128),
     P.W.scaled(P.W.WORKLOADS["gptoss_fp8xfp4"], T=8500, H=256, I=128, E=128),
 ]
