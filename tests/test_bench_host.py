@@ -77,9 +77,9 @@ def test_traffic_digest_ignores_comments_but_not_code(tmp_path, monkeypatch):
     f.write_text(text.replace("// Grouped block-scaled GEMMs", "//   Grouped   GEMMs, reworded") +
                  "\n/* a trailing\n   block comment */\n\n")
     assert bench.kernel_source_digest([src]) == base
-    needle = "kStages = DEC ? 5 : 4"
+    needle = "kThreads = 384;"
     assert needle in text
-    f.write_text(text.replace(needle, "kStages = DEC ? 5 : 3"))
+    f.write_text(text.replace(needle, "kThreads = 256;"))
     assert bench.kernel_source_digest([src]) != base
     f.unlink()
     assert bench.kernel_source_digest([src]) is None
