@@ -29,7 +29,8 @@ definitions that accompany those pages; the readings taken where the pages
 are silent are listed in each module.
 
 Modules:
-  formats  -- exact decode tables and the activation quantizer.
+  formats  -- exact decode tables and the activation quantizers (e4m3 1x128;
+              e2m1 1x32 for the FP4-activation variant).
   routing  -- flatten + stable counting sort + padded grouped layout.
   moe      -- the experts forward itself (per pair, fp64).
 """

@@ -21,11 +21,27 @@ form comes from the workload definitions. Readings taken here:
   saturation to +-448 (never reached by the rule above), and keeps the sign
   of zero (a negative value that rounds to zero gives 0x80);
 * a partial last block (dim % 128 != 0) covers only the existing elements.
+
+FP4 activations (the variant in which both GEMM operands are e2m1, the
+FP4 x FP4 block-scaled MMA named next to the FP8 x FP4 one): the pages give
+no activation rule for it, so the microscaling blocking of the FP4 weights is
+taken: 1x32 blocks, one UE8M0 exponent per block, e2m1 codes. Readings:
+
+* n = min{n : amax <= 6 * 2^n} (6 is the largest e2m1 magnitude), the same
+  rule as for the FP4 weight data; amax = 0 gives n = 0; n is clamped to
+  [-127, 127];
+* the conversion to e2m1 is round-to-nearest, ties to the even code, with
+  saturation to +-6 (never reached by the rule above), and keeps the sign of
+  zero (a negative value that rounds to zero gives code 0x8);
+* codes are packed two per byte with the even element in the low nibble, as
+  for the FP4 weights.
 """
 import numpy as np
 
 E4M3_MAX = 448.0
 ACT_BLOCK = 128
+E2M1_MAX = 6.0
+ACT_BLOCK_FP4 = 32
 
 
 def _e4m3_value(code):
@@ -149,6 +165,73 @@ def dequantize_rows_1x128(codes, exps):
     D = vals.shape[1]
     scale = np.repeat(np.ldexp(1.0, exps.astype(np.int64)), ACT_BLOCK, axis=1)[:, :D]
     return vals * scale
+
+
+# Non-negative e2m1 magnitudes in code order 0..7 (ascending).
+_E2M1_POS = E2M1_TABLE[:8]
+
+
+def e2m1_rne_satfinite(v):
+    """Round fp64 values to 4-bit e2m1 codes: nearest, ties to even code,
+    saturate at 6; the sign bit (0x8) follows the sign of v, zero included."""
+    v = np.asarray(v, dtype=np.float64)
+    if np.isnan(v).any():
+        raise ValueError("NaN input to the e2m1 quantizer")
+    mag = np.minimum(np.abs(v), E2M1_MAX)
+    hi = np.minimum(np.searchsorted(_E2M1_POS, mag, side="left"), 7)  # first >= mag
+    lo = np.maximum(hi - 1, 0)
+    d_hi = _E2M1_POS[hi] - mag
+    d_lo = mag - _E2M1_POS[lo]
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & ((hi & 1) == 0))
+    exact = _E2M1_POS[hi] == mag
+    code = np.where(exact | pick_hi, hi, lo).astype(np.uint8)
+    return np.where(np.signbit(v), code | 0x8, code).astype(np.uint8)
+
+
+def act_scale_exponent_e2m1(amax):
+    """n = min{n : amax <= 6 * 2^n}, 0 for amax == 0, clamped to [-127, 127].
+
+    With amax = m * 2^E (m in [0.5, 1), numpy.frexp) and 6 = 0.75 * 2^3:
+    amax <= 0.75 * 2^(3+n)  <=>  n >= E - 3 when m <= 0.75, else n >= E - 2.
+    """
+    amax = np.asarray(amax, dtype=np.float64)
+    m, E = np.frexp(amax)
+    n = np.where(m <= 0.75, E - 3, E - 2)
+    n = np.where(amax == 0, 0, n)
+    return np.clip(n, -127, 127).astype(np.int32)
+
+
+def quantize_rows_1x32_e2m1(x):
+    """Dynamic 1x32 FP4 activation quantization of a 2-D fp64 array.
+
+    Returns (codes uint8 [R, D], one 4-bit code per element, and exps int32
+    [R, ceil(D/32)]) with x ~= E2M1_TABLE[codes] * 2^exps (block-broadcast).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    R, D = x.shape
+    nb = (D + ACT_BLOCK_FP4 - 1) // ACT_BLOCK_FP4
+    codes = np.empty((R, D), dtype=np.uint8)
+    exps = np.empty((R, nb), dtype=np.int32)
+    for b in range(nb):
+        lo, hi = b * ACT_BLOCK_FP4, min(D, (b + 1) * ACT_BLOCK_FP4)
+        blk = x[:, lo:hi]
+        e = act_scale_exponent_e2m1(np.max(np.abs(blk), axis=1))
+        exps[:, b] = e
+        codes[:, lo:hi] = e2m1_rne_satfinite(blk * np.ldexp(1.0, -e)[:, None])
+    return codes, exps
+
+
+def dequantize_rows_1x32_e2m1(codes, exps):
+    vals = E2M1_TABLE[np.asarray(codes, dtype=np.uint8)]
+    D = vals.shape[1]
+    scale = np.repeat(np.ldexp(1.0, exps.astype(np.int64)), ACT_BLOCK_FP4, axis=1)[:, :D]
+    return vals * scale
+
+
+def pack_e2m1(codes):
+    """4-bit codes [R, D] (D even) -> bytes [R, D/2], even element in the low nibble."""
+    c = np.asarray(codes, dtype=np.uint8)
+    return (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
 
 
 def bf16_bits_to_f64(bits):

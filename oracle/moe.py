@@ -29,6 +29,11 @@ Weights are decoded exactly (value = code * scale in fp64):
   one UE8M0 byte per 1x32 block; w13 [E, 2I, H/2], w13_scale [E, 2I, H/32];
   w2 [E, H, I/2], w2_scale [E, H, I/32].
 Rows [0, I) of w13 are the gate half and rows [I, 2I) the up half.
+
+``act_fmt`` selects the activation format of steps 2 and 5: "fp8" (e4m3,
+1x128 blocks, the pages' dynamic rule) or "fp4" (e2m1, 1x32 blocks with
+UE8M0 exponents, for the variant in which both GEMM operands are FP4; the
+rule is in ``oracle.formats``). Everything else is the same.
 """
 import numpy as np
 
@@ -37,6 +42,24 @@ from .routing import route
 
 FP8 = "fp8"
 FP4 = "fp4"
+ACT_FMTS = (FP8, FP4)
+
+
+def quantize_act(x, act_fmt):
+    """Steps 2 and 5: (codes, exps) of fp64 rows in the activation format."""
+    if act_fmt == FP8:
+        return F.quantize_rows_1x128(x)
+    if act_fmt == FP4:
+        return F.quantize_rows_1x32_e2m1(x)
+    raise ValueError(act_fmt)
+
+
+def dequantize_act(codes, exps, act_fmt):
+    if act_fmt == FP8:
+        return F.dequantize_rows_1x128(codes, exps)
+    if act_fmt == FP4:
+        return F.dequantize_rows_1x32_e2m1(codes, exps)
+    raise ValueError(act_fmt)
 
 
 def dequant_weight(fmt, w, scale, expert, rows, cols):
@@ -63,34 +86,37 @@ def swiglu(h, inter, limit):
     return g / (1.0 + np.exp(-g)) * u
 
 
-def expert_mlp(xd, w13d, w2d, inter, limit):
+def expert_mlp(xd, w13d, w2d, inter, limit, act_fmt=FP8):
     """One expert on the dequantized activation rows xd [n, H] (fp64).
 
     Returns (y [n, H], act codes, act exps) where act = requantized SwiGLU.
     """
     h = xd @ w13d.T
     a = swiglu(h, inter, limit)
-    aq, ae = F.quantize_rows_1x128(a)
-    y = F.dequantize_rows_1x128(aq, ae) @ w2d.T
+    aq, ae = quantize_act(a, act_fmt)
+    y = dequantize_act(aq, ae, act_fmt) @ w2d.T
     return y, aq, ae
 
 
 def experts_forward(hidden_bits, topk_idx, topk_w, weights, swiglu_limit=None,
-                    tokens=None, return_taps=False):
+                    tokens=None, return_taps=False, act_fmt=FP8):
     """fp64 experts forward for the tokens listed in ``tokens`` (default all).
 
     hidden_bits: uint16 bf16 bit patterns [T, H]; topk_idx: int [T, K];
     topk_w: float32 [T, K]; weights: dict(fmt, E, H, I, w13, w13_scale, w2,
-    w2_scale). Returns out [len(tokens), H] in fp64 (and taps if asked).
+    w2_scale); act_fmt: "fp8" or "fp4" (FP4 weights only). Returns out
+    [len(tokens), H] in fp64 (and taps if asked).
     """
+    if act_fmt == FP4 and weights["fmt"] != FP4:
+        raise ValueError("FP4 activations are defined with FP4 weights")
     fmt, E, H, I = weights["fmt"], weights["E"], weights["H"], weights["I"]
     topk_idx = np.asarray(topk_idx, dtype=np.int64)
     topk_w = np.asarray(topk_w, dtype=np.float32).astype(np.float64)
     T, K = topk_idx.shape
     tokens = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
     x = F.bf16_bits_to_f64(np.asarray(hidden_bits)[tokens])
-    xq, xe = F.quantize_rows_1x128(x)
-    xd = F.dequantize_rows_1x128(xq, xe)
+    xq, xe = quantize_act(x, act_fmt)
+    xd = dequantize_act(xq, xe, act_fmt)
 
     # Per-pair outputs y[(i, k)] for the selected tokens; skipped slots never
     # produce a row, so they contribute exactly zero below.
@@ -103,7 +129,7 @@ def experts_forward(hidden_bits, topk_idx, topk_w, weights, swiglu_limit=None,
         pairs = np.argwhere(ids == e)  # (i, k), row-major = ascending slot
         w13d = dequant_weight(fmt, weights["w13"], weights["w13_scale"], e, 2 * I, H)
         w2d = dequant_weight(fmt, weights["w2"], weights["w2_scale"], e, H, I)
-        ye, aq, ae = expert_mlp(xd[pairs[:, 0]], w13d, w2d, I, swiglu_limit)
+        ye, aq, ae = expert_mlp(xd[pairs[:, 0]], w13d, w2d, I, swiglu_limit, act_fmt)
         for j, (i, k) in enumerate(pairs):
             y[(i, k)] = ye[j]
             act[(i, k)] = (aq[j], ae[j])
@@ -119,10 +145,10 @@ def experts_forward(hidden_bits, topk_idx, topk_w, weights, swiglu_limit=None,
     return out
 
 
-def quantize_hidden(hidden_bits):
-    """Step 2 alone on every token: (codes [T, H], exps [T, ceil(H/128)])."""
-    return F.quantize_rows_1x128(F.bf16_bits_to_f64(hidden_bits))
+def quantize_hidden(hidden_bits, act_fmt=FP8):
+    """Step 2 alone on every token: (codes [T, H], exps [T, blocks])."""
+    return quantize_act(F.bf16_bits_to_f64(hidden_bits), act_fmt)
 
 
-__all__ = ["FP8", "FP4", "route", "experts_forward", "quantize_hidden",
-           "dequant_weight", "swiglu", "expert_mlp"]
+__all__ = ["FP8", "FP4", "ACT_FMTS", "route", "experts_forward", "quantize_hidden", "quantize_act",
+           "dequantize_act", "dequant_weight", "swiglu", "expert_mlp"]

@@ -69,6 +69,37 @@ def _quant_dequant(row):
     return out
 
 
+_E2M1_MAG = [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+
+
+def _round_e2m1(v):
+    """Nearest e2m1 value (same sign), ties to the even code, saturating at 6."""
+    m = min(abs(v), 6.0)
+    d = [abs(m - c) for c in _E2M1_MAG]
+    best = [c for c in range(8) if d[c] == min(d)]
+    even = [c for c in best if c % 2 == 0]
+    return math.copysign(_E2M1_MAG[(even or best)[0]], v)
+
+
+def _exp_rule_fp4(amax):
+    if amax == 0:
+        return 0
+    for n in range(-127, 128):
+        if amax <= 6.0 * 2.0 ** n:
+            return n
+    return 127
+
+
+def _quant_dequant_fp4(row):
+    out = np.empty(len(row))
+    for b0 in range(0, len(row), 32):
+        blk = row[b0:b0 + 32]
+        n = _exp_rule_fp4(max(abs(v) for v in blk))
+        for j, v in enumerate(blk):
+            out[b0 + j] = _round_e2m1(v / 2.0 ** n) * 2.0 ** n
+    return out
+
+
 def _weight(fmt, w, s, e, r, c):
     if fmt == "fp8":
         return _E4M3[int(w[e, r, c])] * float(s[e, r // 128, c // 128])
@@ -78,8 +109,9 @@ def _weight(fmt, w, s, e, r, c):
     return (-mag if code & 8 else mag) * 2.0 ** (int(s[e, r, c // 32]) - 127)
 
 
-def brute_force(bits, idx, topk_w, wt, limit):
+def brute_force(bits, idx, topk_w, wt, limit, act="fp8"):
     fmt, E, H, I = wt["fmt"], wt["E"], wt["H"], wt["I"]
+    qd = _quant_dequant_fp4 if act == "fp4" else _quant_dequant
     T, K = idx.shape
     W13 = np.array([[[_weight(fmt, wt["w13"], wt["w13_scale"], e, r, c) for c in range(H)]
                      for r in range(2 * I)] for e in range(E)])
@@ -87,7 +119,7 @@ def brute_force(bits, idx, topk_w, wt, limit):
                     for r in range(H)] for e in range(E)])
     out = np.zeros((T, H))
     for t in range(T):
-        x = _quant_dequant([_bf16(b) for b in bits[t]])
+        x = qd([_bf16(b) for b in bits[t]])
         for e in range(E):
             r = sum(float(np.float32(topk_w[t, k])) for k in range(K) if idx[t, k] == e)
             if not any(idx[t, k] == e for k in range(K)):
@@ -97,17 +129,17 @@ def brute_force(bits, idx, topk_w, wt, limit):
             if limit is not None:
                 g = np.minimum(g, limit)
                 u = np.clip(u, -limit, limit)
-            a = _quant_dequant(list(g / (1 + np.exp(-g)) * u))
+            a = qd(list(g / (1 + np.exp(-g)) * u))
             out[t] += r * (W2[e] @ a)
     return out
 
 
-def _case(T, H, I, E, K, fmt, skip=0.0, limit=None, seed=3):
+def _case(T, H, I, E, K, fmt, skip=0.0, limit=None, seed=3, act="fp8"):
     wl = W.Workload("pin", T, H, I, E, K, fmt, "softmax", skip_frac=skip, swiglu_limit=limit, seed=seed)
     hid, idx, w, wt = W.make_all(wl)
     bits = hid.view(torch.int16).numpy().view(np.uint16)
     wt = {k: (v.numpy() if torch.is_tensor(v) else v) for k, v in wt.items()}
-    return bits, idx.numpy(), w.numpy(), wt, limit
+    return bits, idx.numpy(), w.numpy(), wt, limit, act
 
 
 def _rel(a, b):
@@ -117,16 +149,24 @@ def _rel(a, b):
 CASES = [dict(T=3, H=128, I=128, E=3, K=2, fmt="fp8", skip=0.2),
          dict(T=2, H=256, I=128, E=2, K=2, fmt="fp8", limit=0.05),
          dict(T=3, H=128, I=64, E=3, K=2, fmt="fp4", skip=0.2),
-         dict(T=2, H=192, I=96, E=2, K=1, fmt="fp4", limit=0.02)]
+         dict(T=2, H=192, I=96, E=2, K=1, fmt="fp4", limit=0.02),
+         dict(T=3, H=128, I=64, E=3, K=2, fmt="fp4", skip=0.2, act="fp4"),
+         dict(T=2, H=192, I=96, E=2, K=2, fmt="fp4", limit=0.02, act="fp4")]
 
 
 @pytest.mark.parametrize("case", CASES)
 def test_oracle_matches_brute_force(case):
-    bits, idx, w, wt, limit = _case(**case)
-    ref = brute_force(bits, idx, w, wt, limit)
-    got = M.experts_forward(bits, idx, w, wt, limit)
+    bits, idx, w, wt, limit, act = _case(**case)
+    ref = brute_force(bits, idx, w, wt, limit, act)
+    got = M.experts_forward(bits, idx, w, wt, limit, act_fmt=act)
     assert np.abs(ref).max() > 0
     assert _rel(got, ref) < 1e-12
+
+
+def test_fp4_activations_need_fp4_weights():
+    bits, idx, w, wt, limit, _ = _case(**CASES[0])
+    with pytest.raises(ValueError):
+        M.experts_forward(bits, idx, w, wt, limit, act_fmt="fp4")
 
 
 # ----------------------------------------------------------------- closed forms
@@ -186,13 +226,13 @@ def test_clamp_closed_form():
 
 
 def test_all_skipped_is_exact_zero():
-    bits, idx, w, wt, _ = _case(4, 128, 128, 3, 2, "fp8")
+    bits, idx, w, wt, _, _ = _case(4, 128, 128, 3, 2, "fp8")
     out = M.experts_forward(bits, np.full_like(idx, -1), w, wt)
     assert np.array_equal(out, np.zeros_like(out)) and not np.signbit(out).any()
 
 
 def test_nan_weight_in_skipped_slot_has_no_effect():
-    bits, idx, w, wt, _ = _case(4, 128, 128, 3, 2, "fp8")
+    bits, idx, w, wt, _, _ = _case(4, 128, 128, 3, 2, "fp8")
     idx[1, 0] = -1
     w2 = w.copy()
     w2[1, 0] = np.nan
@@ -202,7 +242,7 @@ def test_nan_weight_in_skipped_slot_has_no_effect():
 
 
 def test_padding_tokens_leave_outputs_unchanged():
-    bits, idx, w, wt, _ = _case(4, 128, 128, 3, 2, "fp8")
+    bits, idx, w, wt, _, _ = _case(4, 128, 128, 3, 2, "fp8")
     pad_bits = np.concatenate([bits, bits[:2]])
     pad_idx = np.concatenate([idx, np.full((2, 2), -1, idx.dtype)])
     pad_w = np.concatenate([w, w[:2]])
@@ -212,7 +252,7 @@ def test_padding_tokens_leave_outputs_unchanged():
 
 
 def test_token_subset_equals_full_rows():
-    bits, idx, w, wt, _ = _case(6, 128, 128, 3, 2, "fp4")
+    bits, idx, w, wt, _, _ = _case(6, 128, 128, 3, 2, "fp4")
     full = M.experts_forward(bits, idx, w, wt)
     sub = M.experts_forward(bits, idx, w, wt, tokens=[4, 1])
     assert np.array_equal(sub, full[[4, 1]])
@@ -252,24 +292,55 @@ def _exp_off_by_one(x):
     return codes, exps + 1  # exponent stored one step too large
 
 
+_orig_quant_fp4 = F.quantize_rows_1x32_e2m1
+
+
+def _fp4_exp_off_by_one(x):
+    codes, exps = _orig_quant_fp4(x)
+    return codes, exps - 1  # exponent stored one step too small
+
+
+def _fp4_ties_away(v):
+    """e2m1 rounding with ties away from zero instead of to the even code."""
+    v = np.asarray(v, dtype=np.float64)
+    mags = F.E2M1_TABLE[:8]
+    m = np.minimum(np.abs(v), 6.0)[..., None]
+    d = np.abs(m - mags)
+    pick = (d == d.min(axis=-1, keepdims=True)) * np.arange(8)
+    return (pick.max(axis=-1) | np.where(np.signbit(v), 8, 0)).astype(np.uint8)
+
+
+def _fp4_block_64(x):
+    monkey = F.ACT_BLOCK_FP4
+    try:
+        F.ACT_BLOCK_FP4 = 64
+        codes, exps = _orig_quant_fp4(x)
+    finally:
+        F.ACT_BLOCK_FP4 = monkey
+    return codes, np.repeat(exps, 2, axis=1)[:, :(x.shape[1] + 31) // 32]
+
+
 @pytest.mark.parametrize("name,target,attr,bad,case", [
     ("gate/up swapped", M, "swiglu", _swap_halves, CASES[0]),
     ("clamp dropped", M, "swiglu", _no_clamp, CASES[1]),
     ("one scale per row block", M, "dequant_weight", _first_kblock_scale, CASES[1]),
     ("fp4 nibbles swapped", M, "dequant_weight", _nibbles_swapped, CASES[2]),
     ("scale exponent off by one", F, "quantize_rows_1x128", _exp_off_by_one, CASES[0]),
+    ("fp4 activation exponent off by one", F, "quantize_rows_1x32_e2m1", _fp4_exp_off_by_one, CASES[4]),
+    ("fp4 activation blocks of 64", F, "quantize_rows_1x32_e2m1", _fp4_block_64, CASES[5]),
+    ("fp4 activation ties away from zero", F, "e2m1_rne_satfinite", _fp4_ties_away, CASES[4]),
 ])
 def test_planted_mistake_is_caught(monkeypatch, name, target, attr, bad, case):
-    bits, idx, w, wt, limit = _case(**case)
-    ref = brute_force(bits, idx, w, wt, limit)
+    bits, idx, w, wt, limit, act = _case(**case)
+    ref = brute_force(bits, idx, w, wt, limit, act)
     monkeypatch.setattr(target, attr, bad)
-    got = M.experts_forward(bits, idx, w, wt, limit)
+    got = M.experts_forward(bits, idx, w, wt, limit, act_fmt=act)
     assert _rel(got, ref) > 1e-6, name
 
 
 def test_planted_weight_drop_is_caught():
-    bits, idx, w, wt, limit = _case(**CASES[0])
-    ref = brute_force(bits, idx, w, wt, limit)
+    bits, idx, w, wt, limit, act = _case(**CASES[0])
+    ref = brute_force(bits, idx, w, wt, limit, act)
     got = M.experts_forward(bits, idx, np.ones_like(w), wt, limit)
     assert _rel(got, ref) > 1e-3
 
