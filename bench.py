@@ -45,6 +45,9 @@ DEFAULT_WORKLOAD = "dsv3_prefill_fp8"
 FP8_PEAK_RECORD = os.path.join(ROOT, "profiles", "fp8_peak.json")
 STAGES = ["route", "quant", "gemm1", "gemm2", "combine"]
 L2_FLUSH_BYTES = 256 << 20
+# nominal dense tensor rates of a GB300: fp4 13.5 PF against fp8 4.5 PF
+FP4_OVER_FP8 = 3.0
+ACT_NAME = {"fp8": "e4m3 1x128", "fp4": "e2m1 1x32"}
 CPU_SAMPLE_TOKENS = {"mixtral_prefill_fp8": 24, "dsv3_prefill_fp8": 12, "dsv3_decode_fp8": 6, "gptoss_fp8xfp4": 24}
 
 
@@ -163,8 +166,12 @@ def launches_per_forward(wl):
     routing + quantization (one fused kernel up to 256 slots; else one routing
     kernel up to 8192 slots or histogram + scan + scatter, then the
     quantization kernel), GEMM1, GEMM2, and the combine (inside GEMM2 for FP4
-    weights with at most 8 pairs per expert and at most 256 slots)."""
+    weights with at most 8 pairs per expert and at most 256 slots). With FP4
+    activations routing and quantization are always separate kernels and the
+    GEMMs always run 128-row tiles (no decode mode)."""
     S = wl.T * wl.K
+    if wl.act_fmt == "fp4":
+        return (2 if S <= 8192 else 4) + 2 + 1
     if wl.fmt == "fp4" and S <= 8 * wl.E and S <= 32:
         return 1  # the single-launch decode forward
     front = 1 if S <= 256 else (2 if S <= 8192 else 4)
@@ -259,7 +266,7 @@ def cpu_baseline(wl, hidden, idx, w, weights, n_tok):
     bits_full = np.zeros((len(toks), wl.H), np.uint16)
     bits_full[:] = bits
     t0 = time.perf_counter()
-    OM.experts_forward(bits_full, ids, ws, wts, wl.swiglu_limit)
+    OM.experts_forward(bits_full, ids, ws, wts, wl.swiglu_limit, act_fmt=wl.act_fmt)
     dt = time.perf_counter() - t0
     pairs, _ = routing_stats(ids, wl.E)
     cores = len(os.sched_getaffinity(0))
@@ -314,7 +321,7 @@ def _reference_line(args, wl, ws):
     for step in range(args.warmup + args.steps):
         t = step % small.T
         t0 = time.perf_counter()
-        OM.experts_forward(bits, ids, wv, wts, wl.swiglu_limit, tokens=[t])
+        OM.experts_forward(bits, ids, wv, wts, wl.swiglu_limit, tokens=[t], act_fmt=wl.act_fmt)
         dt = time.perf_counter() - t0
         if step >= args.warmup:
             times.append(dt)
@@ -333,8 +340,8 @@ def _reference_line(args, wl, ws):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
             "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "K": wl.K,
-                       "weights": wl.fmt, "swiglu_limit": wl.swiglu_limit, "pairs": full_pairs,
-                       "touched_experts": full_touched, "parallelism": f"replicas{ws}",
+                       "weights": wl.fmt, "activations": ACT_NAME[wl.act_fmt], "swiglu_limit": wl.swiglu_limit,
+                       "pairs": full_pairs, "touched_experts": full_touched, "parallelism": f"replicas{ws}",
                        "l2": "not applicable: the oracle runs on the host"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": f"one token of {wl.name} per step (synthetic expert weights), fp64 numpy"},
@@ -360,11 +367,11 @@ def run_ours(args, wl):
     # The one-shot weight transform, timed on its own (not part of a step).
     p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     p0.record()
-    prepared = B.prepare_weights(weights)
+    prepared = B.prepare_weights(weights, activations=wl.act_fmt)
     p1.record()
     torch.cuda.synchronize()
     prepare_ms = p0.elapsed_time(p1)
-    ws = torch.empty(B.workspace_bytes(wl.fmt, wl.T, wl.H, wl.I, wl.E, wl.K), dtype=torch.uint8, device=dev)
+    ws = torch.empty(B.workspace_bytes(prepared.fmt, wl.T, wl.H, wl.I, wl.E, wl.K), dtype=torch.uint8, device=dev)
     out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
     pairs, touched = routing_stats(idx.cpu().numpy(), wl.E)
     flops = 6.0 * wl.H * wl.I * pairs
@@ -508,10 +515,13 @@ def run_ours(args, wl):
         frac_1 = 2.0 / 3.0 if dom == "gemm1" else 1.0 / 3.0
         kflops = flops * frac_1
         wb = weight_bytes_per_expert(wl, 13 if dom == "gemm1" else 2) * touched
+        # activation rows: e4m3 codes (e2m1, two per byte, with FP4
+        # activations) plus one 4-byte scale word per 128 columns
+        per = 2 if wl.act_fmt == "fp4" else 1
         if dom == "gemm1":
-            act = pairs * (wl.H + 4 * ((wl.H + 127) // 128)) + pairs * (wl.I + 4 * ((wl.I + 127) // 128))
+            act = pairs * (wl.H // per + 4 * ((wl.H + 127) // 128)) + pairs * (wl.I // per + 4 * ((wl.I + 127) // 128))
         else:
-            act = pairs * (wl.I + 4 * ((wl.I + 127) // 128)) + pairs * wl.H * 4
+            act = pairs * (wl.I // per + 4 * ((wl.I + 127) // 128)) + pairs * wl.H * 4
         kbytes = wb + act
     peak_tc_2x = 2.0 * peaks["bf16_tflops"]  # fp8 dense = 2 x bf16 dense (nominal 4.5 / 2.25 PF)
     fp8 = load_fp8_peak()
@@ -522,6 +532,12 @@ def run_ours(args, wl):
     else:
         peak_tc = peak_tc_2x
         tc_src = f"{peak_src}: 2 x bf16 burst (fp8/bf16 nominal ratio 2)"
+    if wl.act_fmt == "fp4":
+        # e2m1 x e2m1 runs at the FP4 tensor rate: the FP8 figure above times
+        # the nominal FP4 / FP8 dense ratio (13.5 / 4.5 PF)
+        peak_tc *= FP4_OVER_FP8
+        peak_tc_2x *= FP4_OVER_FP8
+        tc_src = f"fp4 = {FP4_OVER_FP8:g} x ({tc_src}), the nominal dense fp4/fp8 ratio"
     peak_hbm = peaks["hbm_gbs"]
     t_tc = kflops / (peak_tc * 1e12)
     t_hbm = kbytes / (peak_hbm * 1e9)
@@ -556,10 +572,12 @@ def run_ours(args, wl):
     line = {"metric": METRIC, "value": replica_throughput(flops, world, ms_step * 1e-3) / 1e12, "unit": UNIT,
             "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if wl.fmt == "fp8" else "e4m3xe2m1",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "e2m1" if wl.act_fmt == "fp4" else ("e4m3" if wl.fmt == "fp8" else "e4m3xe2m1"),
             "data": "synthetic",
             "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "K": wl.K,
-                       "weights": wl.fmt, "swiglu_limit": wl.swiglu_limit, "pairs": pairs,
+                       "weights": wl.fmt, "activations": ACT_NAME[wl.act_fmt], "swiglu_limit": wl.swiglu_limit,
+                       "pairs": pairs,
                        "touched_experts": touched, "parallelism": f"replicas{world}",
                        "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, then a "
                              f"{L2_FLUSH_BYTES >> 20} MiB read); expert weights also exceed L2"},

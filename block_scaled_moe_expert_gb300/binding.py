@@ -21,7 +21,10 @@ LIB_PATH = os.path.join(HERE, "libbsmoe.so")
 
 MOE_W_FP8 = 0
 MOE_W_FP4 = 1
-FMT = {"fp8": MOE_W_FP8, "fp4": MOE_W_FP4}
+MOE_W_FP4_ACT_FP4 = 2
+# format names of the prepared weights: the weight format, and for FP4
+# weights used with FP4 activations "fp4_act_fp4"
+FMT = {"fp8": MOE_W_FP8, "fp4": MOE_W_FP4, "fp4_act_fp4": MOE_W_FP4_ACT_FP4}
 
 MOE_OK = 0
 MOE_DEV_BAD_EXPERT_ID = 0x1
@@ -126,12 +129,24 @@ class PreparedWeights:
         self.fmt, self.E, self.H, self.I = fmt, E, H, I
         self.w13_prep, self.w2_prep = w13_prep, w2_prep
 
+    @property
+    def act_fmt(self):
+        return "fp4" if self.fmt == "fp4_act_fp4" else "fp8"
 
-def prepare_weights(weights, transposed=False):
+
+def prepare_weights(weights, transposed=False, activations="fp8"):
     """weights: dict(fmt, E, H, I, w13, w13_scale, w2, w2_scale) of CUDA tensors,
     K-major ([E, N, K]) or, with transposed=True, N-major ([E, K, N]; see
-    moe_prepare_weights_transposed for the exact shapes)."""
+    moe_prepare_weights_transposed for the exact shapes). activations="fp4"
+    (FP4 weights only) selects the FP4 x FP4 variant for every forward with
+    these prepared weights: e2m1 activations in 1x32 blocks."""
     fmt, E, H, I = weights["fmt"], weights["E"], weights["H"], weights["I"]
+    if activations not in ("fp8", "fp4"):
+        raise ValueError(f"activations must be 'fp8' or 'fp4', got {activations!r}")
+    if activations == "fp4":
+        if fmt != "fp4":
+            raise ValueError("FP4 activations are available with FP4 weights only")
+        fmt = "fp4_act_fp4"
     ts = [weights[k].contiguous() for k in ("w13", "w13_scale", "w2", "w2_scale")]
     _same_device(*ts)
     L = lib()

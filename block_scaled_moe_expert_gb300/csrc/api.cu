@@ -23,7 +23,7 @@ namespace bsmoe {
 namespace {
 
 bool shape_ok(int fmt, int H, int I, int E) {
-  if (fmt != MOE_W_FP8 && fmt != MOE_W_FP4) return false;
+  if (fmt != MOE_W_FP8 && fmt != MOE_W_FP4 && fmt != MOE_W_FP4_ACT_FP4) return false;
   if (E < 1 || E > kMaxExperts) return false;
   if (H < 128 || I < 128 || H > 32768 || I > 32768) return false;
   if (H % 64 || I % 64) return false;
@@ -152,9 +152,11 @@ bool ws_layout(int fmt, int T, int H, int I, int E, int K, WsLayout* out) {
   p.perm = take(4ull * S);
   p.inv = take(4ull * S);
   p.row_slot = take(4ull * M);
-  p.xq = take(static_cast<size_t>(M) * g1.Kp);
+  // e4m3 activations: a byte per element; e2m1 (FP4 activations): two per byte
+  const size_t per_byte = (fmt == MOE_W_FP4_ACT_FP4) ? 2 : 1;
+  p.xq = take(static_cast<size_t>(M) * g1.Kp / per_byte);
   p.xsf = take(4ull * M * g1.KB);
-  p.act = take(static_cast<size_t>(M) * g2.Kp);
+  p.act = take(static_cast<size_t>(M) * g2.Kp / per_byte);
   p.asf = take(4ull * M * g2.KB);
   p.y = take(4ull * M * H);
   L.row_w = take(4ull * M);
@@ -307,17 +309,21 @@ moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, cons
   const GemmGeom g1 = geom_w13(H, I), g2 = geom_w2(H, I);
   const PrepLayout P1 = prep_layout(fmt, E, g1), P2 = prep_layout(fmt, E, g2);
   const bool fp4 = (fmt == MOE_W_FP4);
+  // FP4 activations: both operands stay packed in shared memory (plain byte
+  // maps over K / 2 bytes a row, 128-byte boxes = 256 codes).
+  const bool mx = (fmt == MOE_W_FP4_ACT_FP4);
   // FP4 weights with few pairs per expert: the weight-streaming decode mode
   // of the grouped GEMMs (32-row token chunks, five weight stages).
   const bool decode = decode_mode(fmt, L.S, E);
   const int a_box = decode ? kChunkRows : kBlockM;
+  const uint64_t k1 = mx ? g1.Kp / 2 : g1.Kp, k2 = mx ? g2.Kp / 2 : g2.Kp;
 
   CUtensorMap ta1, tb1, ta2, tb2;
-  if (!make_tmap(&ta1, false, ws + p.xq, g1.Kp, L.M, a_box) ||
-      !make_tmap(&tb1, fp4, static_cast<const uint8_t*>(w13_prep) + P1.codes_off, g1.Kp,
+  if (!make_tmap(&ta1, false, ws + p.xq, k1, L.M, a_box) ||
+      !make_tmap(&tb1, fp4, static_cast<const uint8_t*>(w13_prep) + P1.codes_off, k1,
                  static_cast<uint64_t>(E) * g1.Np, kBlockN) ||
-      !make_tmap(&ta2, false, ws + p.act, g2.Kp, L.M, a_box) ||
-      !make_tmap(&tb2, fp4, static_cast<const uint8_t*>(w2_prep) + P2.codes_off, g2.Kp,
+      !make_tmap(&ta2, false, ws + p.act, k2, L.M, a_box) ||
+      !make_tmap(&tb2, fp4, static_cast<const uint8_t*>(w2_prep) + P2.codes_off, k2,
                  static_cast<uint64_t>(E) * g2.Np, kBlockN))
     return MOE_ERR_CUDA;
 
@@ -344,7 +350,7 @@ moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, cons
   a1.w_scale = static_cast<const uint8_t*>(w13_prep) + P1.scale_off;
   a1.out_q = ws + p.act;
   a1.out_sf = ws + p.asf;
-  a1.out_cols = g2.Kp;
+  a1.out_cols = mx ? g2.Kp / 2 : g2.Kp;
   a1.out_blocks = g2.KB;
   a1.act_f32 = act_f32;
   a1.g = g1;
@@ -376,14 +382,14 @@ moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, cons
       if (!mark(i)) return MOE_ERR_CUDA;
     return MOE_OK;
   }
-  if (L.S <= kFusedRouteQuantSlots) {
+  if (L.S <= kFusedRouteQuantSlots && !mx) {
     // One launch for both (the quant stage then has zero length).
     if (launch_route_quant_small(topk_idx, hidden, topk_w, T, H, E, K, L, ws, out, st) != cudaSuccess || !mark(1) ||
         !mark(2))
       return MOE_ERR_CUDA;
   } else {
     if (launch_route(topk_idx, L.S, E, L, ws, st) != cudaSuccess || !mark(1)) return MOE_ERR_CUDA;
-    if (launch_quant(hidden, topk_w, T, H, K, L, ws, st) != cudaSuccess || !mark(2)) return MOE_ERR_CUDA;
+    if (launch_quant(fmt, hidden, topk_w, T, H, K, L, ws, st) != cudaSuccess || !mark(2)) return MOE_ERR_CUDA;
   }
 
   if (launch_gemm(fmt, true, decode, ta1, tb1, a1, d.sms, st) != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;

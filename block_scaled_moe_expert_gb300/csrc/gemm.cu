@@ -60,6 +60,12 @@ constexpr int kScaleGroup = 4;          // FP8: K blocks per slot
 constexpr uint32_t kSwBytes = 32;       // FP8: 8 weight scales (one per 32 columns) per K block
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfTmemCol = 256;  // FP4: per stage 4 SFA + 8 SFB columns from here
+// FP4 x FP4 (FP4 activations): a stage spans K = 256 (128 bytes of packed
+// codes a row, the SWIZZLE_128B row, like an FP8 stage), i.e. two 128-K
+// scale chunks: 8 SFA + 16 SFB TMEM columns per stage.
+constexpr int kMx = MOE_W_FP4_ACT_FP4;
+template <int FMT>
+constexpr uint32_t kSfColsPerStage = FMT == kMx ? 24 : 12;
 
 // Pipeline shape. Tile mode: a work unit is a 128-row token tile; a stage
 // holds its 16 KB of activation rows and a 32 KB weight tile (4 stages).
@@ -79,15 +85,17 @@ struct Pipe {
 
 constexpr uint32_t kYBoxBytes = 32 * 16 * 4;
 
-template <bool DEC>
+template <bool DEC, int FMT>
 struct __align__(1024) SmemT {
+  static constexpr int kSfChunks = FMT == kMx ? 2 : 1;  // 128-K scale chunks a stage
+  static constexpr int kSlots = FMT == kMx ? 1 : kScaleSlots;  // FP8 promotion-scale ring (FP8 only)
   uint8_t b[Pipe<DEC>::kStages][kTileBBytes];
   uint8_t a[Pipe<DEC>::kARegion];  // stage s at s * kAStride (1024-byte aligned)
   // GEMM2 in tile mode: per epilogue warp, a 32-row x 16-column fp32 box
   // through which its row stores are transposed (tile mode only).
   uint8_t ystage[DEC ? 16 : kEpiThreads / 32 * kYBoxBytes];
-  uint8_t sfa[Pipe<DEC>::kStages][kSfaBytes];
-  uint8_t sfb[Pipe<DEC>::kStages][kSfbBytes];
+  uint8_t sfa[Pipe<DEC>::kStages][kSfChunks * kSfaBytes];
+  uint8_t sfb[Pipe<DEC>::kStages][kSfChunks * kSfbBytes];
   uint64_t full[Pipe<DEC>::kStages];
   uint64_t empty[Pipe<DEC>::kStages];
   uint64_t tfull[2];
@@ -96,8 +104,8 @@ struct __align__(1024) SmemT {
   // FP8 promotion scales, filled by the producer and released by the
   // epilogue (its own ring: the MMA frees the operand stages before the
   // epilogue reads the scales of that K block).
-  uint32_t sfa_w[kScaleSlots][kScaleGroup][kBlockM];
-  float sw[kScaleSlots][kScaleGroup][8];
+  uint32_t sfa_w[kSlots][kScaleGroup][kBlockM];
+  float sw[kSlots][kScaleGroup][8];
   uint64_t sfull[kScaleSlots];
   uint64_t sempty[kScaleSlots];
   uint32_t tmem_base;
@@ -105,14 +113,16 @@ struct __align__(1024) SmemT {
   __device__ uint8_t* a_stage(int s) { return a + s * Pipe<DEC>::kAStride; }
 };
 
-template <bool DEC>
+template <bool DEC, int FMT>
 constexpr bool smem_layout_ok() {
-  return offsetof(SmemT<DEC>, a) % 1024 == 0 && Pipe<DEC>::kAStride % 1024 == 0 &&
-         offsetof(SmemT<DEC>, sfa) % 16 == 0 && offsetof(SmemT<DEC>, sfb) % 16 == 0 &&
-         offsetof(SmemT<DEC>, sfa_w) % 16 == 0 && offsetof(SmemT<DEC>, sw) % 16 == 0 &&
-         sizeof(SmemT<DEC>) + 1024 <= 227 * 1024 && kSfTmemCol + Pipe<DEC>::kStages * 12 <= kTmemCols;
+  using S = SmemT<DEC, FMT>;
+  return offsetof(S, a) % 1024 == 0 && Pipe<DEC>::kAStride % 1024 == 0 && offsetof(S, sfa) % 16 == 0 &&
+         offsetof(S, sfb) % 16 == 0 && offsetof(S, sfa_w) % 16 == 0 && offsetof(S, sw) % 16 == 0 &&
+         sizeof(S) + 1024 <= 227 * 1024 && kSfTmemCol + Pipe<DEC>::kStages * kSfColsPerStage<FMT> <= kTmemCols;
 }
-static_assert(smem_layout_ok<false>() && smem_layout_ok<true>(), "shared / tensor memory layout");
+static_assert(smem_layout_ok<false, MOE_W_FP8>() && smem_layout_ok<false, MOE_W_FP4>() &&
+                  smem_layout_ok<true, MOE_W_FP4>() && smem_layout_ok<false, kMx>(),
+              "shared / tensor memory layout");
 
 struct TileCoord {
   int e, mt, nt, row0, valid;
@@ -192,7 +202,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
                                           const RqArgs* rq) {
   static_assert(!DEC || FMT == MOE_W_FP4, "decode mode is built for FP4 weights");
   static_assert(KIND != kBoth || DEC, "the single-launch forward runs the decode mode");
-  using Smem = SmemT<DEC>;
+  using Smem = SmemT<DEC, FMT>;
   constexpr int kStages = Pipe<DEC>::kStages;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned (SWIZZLE_128B atoms). The offset is applied to the
@@ -352,7 +362,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
             kb0 = npre;
           }
         }
-        for (int kb = kb0; kb < KB; ++kb) {
+        // FP4 activations: a stage covers two 128-K blocks (the last one may
+        // hold one: its TMA boxes run past K and read zeros)
+        const int KS = (FMT == kMx) ? (KB + 1) / 2 : KB;
+        for (int kb = kb0; kb < KS; ++kb) {
           if constexpr (KIND == kBoth) {
             // read the next unit's chunk counter ahead (its value is used at
             // that unit's start); placed a few stages in, so that the table
@@ -370,6 +383,18 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
             }
           }
           if (!mbar_wait(&sm.empty[stage], phase ^ 1, abort_flag)) break;
+          if constexpr (FMT == kMx) {
+            const int ch0 = 2 * kb, nch = min(2, KB - ch0);
+            mbar_arrive_expect_tx(&sm.full[stage], kTileABytes + kTileBBytes + nch * (kSfaBytes + kSfbBytes));
+            tma_load_2d(sm.a_stage(stage), TA, &sm.full[stage], kb * 128, c.row0);  // x in bytes
+            tma_load_2d(sm.b[stage], TB, &sm.full[stage], kb * 128, wrow);
+            bulk_load(sm.sfa[stage], A.a_sf + (static_cast<size_t>(c.row0 / kBlockM) * KB + ch0) * kSfaBytes,
+                      nch * kSfaBytes, &sm.full[stage]);
+            bulk_load(sm.sfb[stage], A.w_scale + ((static_cast<size_t>(c.e) * NT + c.nt) * KB + ch0) * kSfbBytes,
+                      nch * kSfbBytes, &sm.full[stage]);
+            if (++stage == kStages) { stage = 0; phase ^= 1; }
+            continue;
+          }
           // weights already in flight from before the dependency wait
           const bool pre = idx == pre_unit && kb < pre_n;
           if (!pre) mbar_arrive_expect_tx(&sm.full[stage], kStageBytes);
@@ -417,6 +442,39 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
             buf ^= 1;
             if (buf == 0) bphase ^= 1;
           }
+        } else if constexpr (FMT == kMx) {
+          // tile mode, one issuing thread
+          if (!mbar_wait(&sm.tempty[0], bphase ^ 1, abort_flag)) break;
+          tc_fence_after();
+          bool ok = true;
+          const int KS = (KB + 1) / 2;
+          for (int ks = 0; ks < KS; ++ks) {
+            if (!mbar_wait(&sm.full[stage], phase, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const int nch = min(2, KB - 2 * ks);
+            const uint32_t sfa_col = kSfTmemCol + stage * kSfColsPerStage<FMT>;
+            const uint32_t sfb_col = sfa_col + 8;
+            for (int ch = 0; ch < nch; ++ch) {
+              tmem_cp_32x128b_warpx4(tbase + sfa_col + 4 * ch,
+                                     smem_desc(smem_u32(sm.sfa[stage] + ch * kSfaBytes), 0, 128, kSwizzleNone));
+              tmem_cp_32x128b_warpx4(tbase + sfb_col + 8 * ch,
+                                     smem_desc(smem_u32(sm.sfb[stage] + ch * kSfbBytes), 0, 128, kSwizzleNone));
+              tmem_cp_32x128b_warpx4(tbase + sfb_col + 8 * ch + 4,
+                                     smem_desc(smem_u32(sm.sfb[stage] + ch * kSfbBytes + 512), 0, 128, kSwizzleNone));
+            }
+            const uint64_t ad = smem_desc(smem_u32(sm.a_stage(stage)), 16, 1024, kSwizzle128B);
+            const uint64_t bd = smem_desc(smem_u32(sm.b[stage]), 16, 1024, kSwizzle128B);
+            // four K = 64 steps of 32 bytes; step j takes scale bytes 2 (j % 2)
+            // and 2 (j % 2) + 1 of chunk j / 2
+            for (int j = 0; j < 2 * nch; ++j)
+              mma_mxf4(tbase, ad + 2 * j, bd + 2 * j, idesc_mxf4(kBlockM, kBlockN, 2 * (j & 1), 2 * (j & 1)),
+                       tbase + sfa_col + 4 * (j >> 1), tbase + sfb_col + 8 * (j >> 1), (ks > 0 || j > 0) ? 1u : 0u);
+            mma_commit(&sm.empty[stage]);
+            if (++stage == kStages) { stage = 0; phase ^= 1; }
+          }
+          if (!ok) break;
+          mma_commit(&sm.tfull[0]);
+          bphase ^= 1;
         } else {
           bool ok = mbar_wait(&sm.tempty[0], bphase ^ 1, abort_flag);
           if constexpr (DEC) ok = __all_sync(0xffffffffu, ok);
@@ -586,7 +644,55 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
         }
       }
       const int row = c.row0 + m;
-      if (GEMM1) {
+      if (FMT == kMx && GEMM1) {
+        // FP4 activations: SwiGLU, then the 1x32 e2m1 rule; a thread's 64
+        // intermediate columns j = 128 nt + 64 wg + i are two whole blocks,
+        // so no exchange between the warpgroups is needed.
+        if (!ok) break;  // warp-uniform
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          float gt = ACC(i), up = ACC(64 + i);
+          if (clamp) {
+            gt = fminf(gt, limit);
+            up = fminf(fmaxf(up, -limit), limit);
+          }
+          ACC(i) = silu_mul(gt, up);
+        }
+        if (m < c.valid) {
+          if (args.act_f32 != nullptr) {
+            // debug tap: the fp32 values requantized below (row stride in elements)
+            float* dst = args.act_f32 + static_cast<size_t>(row) * (2 * args.out_cols) + c.nt * 128 + wg * 64;
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              st_global_v8(dst + 8 * v, __float_as_uint(ACC(8 * v)), __float_as_uint(ACC(8 * v + 1)),
+                           __float_as_uint(ACC(8 * v + 2)), __float_as_uint(ACC(8 * v + 3)),
+                           __float_as_uint(ACC(8 * v + 4)), __float_as_uint(ACC(8 * v + 5)),
+                           __float_as_uint(ACC(8 * v + 6)), __float_as_uint(ACC(8 * v + 7)));
+          }
+          uint32_t pk[8];
+          uint32_t ex = 0;
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {
+            float amax = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(ACC(32 * b + i)));
+            const int e = act_exponent_e2m1(amax);
+            const float s = exp2_neg(e);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int i0 = 32 * b + 8 * u;
+              pk[4 * b + u] = pack8_e2m1(ACC(i0) * s, ACC(i0 + 1) * s, ACC(i0 + 2) * s, ACC(i0 + 3) * s,
+                                         ACC(i0 + 4) * s, ACC(i0 + 5) * s, ACC(i0 + 6) * s, ACC(i0 + 7) * s);
+            }
+            ex |= static_cast<uint32_t>(e + 127) << (8 * b);
+          }
+          st_global_v8(args.out_q + static_cast<size_t>(row) * args.out_cols + c.nt * 64 + wg * 32, pk[0], pk[1],
+                       pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
+          // bytes 2 wg and 2 wg + 1 of the (row, 128-column block nt) scale word
+          reinterpret_cast<uint16_t*>(args.out_sf)[2 * sf_word_index(row, c.nt, args.out_blocks) + wg] =
+              static_cast<uint16_t>(ex);
+        }
+      } else if (GEMM1) {
         // ACC(0..63) = gate, ACC(64..127) = up of intermediate columns
         // j = 128 nt + 64 wg + i.
         float amax = 0.f;
@@ -796,13 +902,13 @@ template <int FMT, bool GEMM1, bool DEC>
 cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args, int num_sms,
                        cudaStream_t st) {
   auto kern = grouped_gemm_kernel<FMT, GEMM1, DEC>;
-  const int smem = static_cast<int>(sizeof(SmemT<DEC>)) + 1024;
+  const int smem = static_cast<int>(sizeof(SmemT<DEC, FMT>)) + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   return launch_kernel(true, kern, num_sms, kThreads, smem, st, ta, tb, args);
 }
 
-static_assert(sizeof(RqSmem<kThreads / 32>) <= sizeof(SmemT<true>::b),
+static_assert(sizeof(RqSmem<kThreads / 32>) <= sizeof(SmemT<true, MOE_W_FP4>::b),
               "the routing + quantization phase borrows the weight ring");
 
 }  // namespace
@@ -811,7 +917,7 @@ cudaError_t launch_single_decode(const CUtensorMap& ta1, const CUtensorMap& tb1,
                                  const CUtensorMap& tb2, const GemmArgs& a1, const GemmArgs& a2, const RqArgs& rq,
                                  int num_sms, cudaStream_t st) {
   auto kern = single_launch_decode_kernel;
-  const int smem = static_cast<int>(sizeof(SmemT<true>)) + 1024;
+  const int smem = static_cast<int>(sizeof(SmemT<true, MOE_W_FP4>)) + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
@@ -840,6 +946,9 @@ cudaError_t launch_gemm(int fmt, bool is_gemm1, bool decode, const CUtensorMap& 
   if (fmt == MOE_W_FP8)
     return is_gemm1 ? launch_one<MOE_W_FP8, true, false>(ta, tb, args, num_sms, st)
                     : launch_one<MOE_W_FP8, false, false>(ta, tb, args, num_sms, st);
+  if (fmt == kMx)
+    return is_gemm1 ? launch_one<kMx, true, false>(ta, tb, args, num_sms, st)
+                    : launch_one<kMx, false, false>(ta, tb, args, num_sms, st);
   if (decode)
     return is_gemm1 ? launch_one<MOE_W_FP4, true, true>(ta, tb, args, num_sms, st)
                     : launch_one<MOE_W_FP4, false, true>(ta, tb, args, num_sms, st);

@@ -107,8 +107,8 @@ cudaError_t launch_kernel(bool dependent, void (*kern)(KArgs...), dim3 grid, dim
 
 // ---------------------------------------------------------------- launches
 cudaError_t launch_route(const int32_t* topk_idx, int S, int E, const WsLayout& L, uint8_t* ws, cudaStream_t st);
-cudaError_t launch_quant(const void* hidden, const float* topk_w, int T, int H, int K, const WsLayout& L, uint8_t* ws,
-                         cudaStream_t st);
+cudaError_t launch_quant(int fmt, const void* hidden, const float* topk_w, int T, int H, int K, const WsLayout& L,
+                         uint8_t* ws, cudaStream_t st);
 // Routing + quantization in one launch, for S = T * K <= kFusedRouteQuantSlots.
 // With the fused combine (below) it also sets that up: per-token valid-slot
 // counts, zeroed arrival counters, and the +0 output rows of tokens whose
@@ -150,10 +150,10 @@ struct GemmArgs {
   const float* row_w;         // GEMM2: routing weight per padded row
   uint32_t* status;
   // outputs
-  uint8_t* out_q;             // GEMM1: e4m3 act [M][act_cols]
+  uint8_t* out_q;             // GEMM1: e4m3 act [M][act_cols] (FP4 activations: e2m1, act_cols / 2 bytes a row)
   uint8_t* out_sf;            // GEMM1: act scale words
   float* out_y;               // GEMM2: f32 [M][H]
-  int out_cols;               // GEMM1: act_cols (= Kp of GEMM2); GEMM2: H
+  int out_cols;               // GEMM1: bytes of an act row (Kp of GEMM2, halved for FP4 activations); GEMM2: H
   int out_blocks;             // GEMM1: act_blocks
   int E, I, H;
   int M;                      // padded row capacity (locates the chunk work list)

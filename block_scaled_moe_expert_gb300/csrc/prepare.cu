@@ -198,7 +198,7 @@ cudaError_t prep_one(int fmt, bool is_w13, bool transposed, int E, int H, int I,
                      uint8_t* out, cudaStream_t st) {
   const GemmGeom g = is_w13 ? geom_w13(H, I) : geom_w2(H, I);
   const PrepLayout L = prep_layout(fmt, E, g);
-  const bool fp4 = (fmt == MOE_W_FP4);
+  const bool fp4 = (fmt != MOE_W_FP8);  // MOE_W_FP4 and MOE_W_FP4_ACT_FP4 share the weights
   const int src_rows = is_w13 ? 2 * I : H;  // N of the original weight
   const int src_k = is_w13 ? H : I;
   const int dst_row_bytes = fp4 ? g.Kp / 2 : g.Kp;

@@ -196,6 +196,19 @@ __device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t adesc, ui
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
+// FP4 x FP4 block-scaled variant: both operands e2m1 packed two per byte in
+// shared memory, K = 64 per instruction, two UE8M0 scale bytes per row of A
+// and of B (one per 32 K), read from TMEM at sfa/sfb starting at the byte the
+// sf ids choose (0 or 2).
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
 // Arrive on an mbarrier once every previously issued tcgen05 op of this
 // thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -244,6 +257,13 @@ __host__ __device__ constexpr uint32_t idesc_f8f6f4(uint32_t afmt, uint32_t bfmt
 __host__ __device__ constexpr uint32_t idesc_mxf8f6f4(uint32_t afmt, uint32_t bfmt, uint32_t M, uint32_t N,
                                                       uint32_t a_sf_id, uint32_t b_sf_id) {
   return (b_sf_id << 4) | (afmt << 7) | (bfmt << 10) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) |
+         (a_sf_id << 29);
+}
+// Instruction descriptor, kind::mxf4: e2m1 x e2m1 (format code 1 of this
+// kind for both), UE8M0 scale factors, sf ids 0 or 2 (the first of the two
+// scale bytes this instruction uses).
+__host__ __device__ constexpr uint32_t idesc_mxf4(uint32_t M, uint32_t N, uint32_t a_sf_id, uint32_t b_sf_id) {
+  return (b_sf_id << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) |
          (a_sf_id << 29);
 }
 

@@ -18,7 +18,9 @@ namespace {
 constexpr int kQuantWarps = 8;
 
 // One CTA per token: gathers the token's valid slots from inv (in ascending
-// k) and quantizes the row into each of their padded rows.
+// k) and quantizes the row into each of their padded rows (kFp4: the e2m1
+// 1x32 rule of the FP4-activation variant).
+template <bool kFp4>
 __global__ void __launch_bounds__(kQuantWarps * 32)
 quant_permute_kernel(const __nv_bfloat16* __restrict__ hidden, const float* __restrict__ topk_w, int H, int K, int Kp,
                      const int32_t* __restrict__ inv, uint8_t* __restrict__ xq, uint32_t* __restrict__ xsf,
@@ -43,7 +45,8 @@ quant_permute_kernel(const __nv_bfloat16* __restrict__ hidden, const float* __re
   }
   __syncthreads();
   if (nrows == 0) return;
-  quantize_token<kQuantWarps, false>(hidden + static_cast<size_t>(t) * H, H, Kp, rows, nrows, xq, xsf, qrow, qsf);
+  quantize_token<kQuantWarps, false, kFp4>(hidden + static_cast<size_t>(t) * H, H, Kp, rows, nrows, xq, xsf, qrow,
+                                           qsf);
 }
 
 // ---------------------------------------------------------------------------
@@ -60,10 +63,11 @@ __global__ void __launch_bounds__(kQuantWarps * 32) route_quant_small_kernel(con
 
 }  // namespace
 
-cudaError_t launch_quant(const void* hidden, const float* topk_w, int T, int H, int K, const WsLayout& L, uint8_t* ws,
-                         cudaStream_t st) {
+cudaError_t launch_quant(int fmt, const void* hidden, const float* topk_w, int T, int H, int K, const WsLayout& L,
+                         uint8_t* ws, cudaStream_t st) {
   const moe_workspace_layout& p = L.pub;
-  return launch_kernel(true, quant_permute_kernel, T, kQuantWarps * 32, 0, st,
+  return launch_kernel(true, fmt == MOE_W_FP4_ACT_FP4 ? quant_permute_kernel<true> : quant_permute_kernel<false>, T,
+                       kQuantWarps * 32, 0, st,
                        reinterpret_cast<const __nv_bfloat16*>(hidden), topk_w, H, K, p.xq_cols,
                        reinterpret_cast<const int32_t*>(ws + p.inv), ws + p.xq, reinterpret_cast<uint32_t*>(ws + p.xsf),
                        reinterpret_cast<float*>(ws + L.row_w));

@@ -62,12 +62,17 @@ constexpr int kLoadBatch = 4;
 // kComplete: wait for the rows' global writes to complete (they are read in
 // the same grid after a grid-wide barrier); otherwise only until the copies
 // have read shared memory (a later kernel reads the rows).
-template <int kNW, bool kComplete>
+// kFp4: the FP4-activation variant's rule instead (1x32 blocks of four lanes,
+// n = min{n : amax <= 6 * 2^n}, e2m1 codes two per byte, so a row is Kp / 2
+// bytes; byte j of a block's scale word is the exponent of its 1x32
+// sub-block j).
+template <int kNW, bool kComplete, bool kFp4 = false>
 __device__ __forceinline__ void quantize_token(const __nv_bfloat16* __restrict__ xr, int H, int Kp,
                                                const int* rows, int n, uint8_t* __restrict__ xq,
                                                uint32_t* __restrict__ xsf, uint8_t* qrow, uint32_t* qsf) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nblk = Kp / 128;
+  const int row_bytes = kFp4 ? Kp / 2 : Kp;
   constexpr int kStep = kNW * 256;
   for (int base = warp * 256; base < Kp; base += kStep * kLoadBatch) {
     uint4 raw[kLoadBatch];
@@ -92,21 +97,33 @@ __device__ __forceinline__ void quantize_token(const __nv_bfloat16* __restrict__
       float amax = 0.f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+      if constexpr (kFp4) {
 #pragma unroll
-      for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      const int e = act_exponent(amax);
-      const float s = exp2_neg(e);
-      if (c0 < Kp) {
-        *reinterpret_cast<uint2*>(qrow + c0) = make_uint2(pack4_e4m3(v[0] * s, v[1] * s, v[2] * s, v[3] * s),
-                                                          pack4_e4m3(v[4] * s, v[5] * s, v[6] * s, v[7] * s));
-        if ((lane & 15) == 0) qsf[c0 / 128] = static_cast<uint32_t>(e + 127) * 0x01010101u;
+        for (int o = 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const int e = act_exponent_e2m1(amax);
+        const float s = exp2_neg(e);
+        if (c0 < Kp) {
+          *reinterpret_cast<uint32_t*>(qrow + c0 / 2) =
+              pack8_e2m1(v[0] * s, v[1] * s, v[2] * s, v[3] * s, v[4] * s, v[5] * s, v[6] * s, v[7] * s);
+          if ((lane & 3) == 0) reinterpret_cast<uint8_t*>(qsf)[c0 / 32] = static_cast<uint8_t>(e + 127);
+        }
+      } else {
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const int e = act_exponent(amax);
+        const float s = exp2_neg(e);
+        if (c0 < Kp) {
+          *reinterpret_cast<uint2*>(qrow + c0) = make_uint2(pack4_e4m3(v[0] * s, v[1] * s, v[2] * s, v[3] * s),
+                                                            pack4_e4m3(v[4] * s, v[5] * s, v[6] * s, v[7] * s));
+          if ((lane & 15) == 0) qsf[c0 / 128] = static_cast<uint32_t>(e + 127) * 0x01010101u;
+        }
       }
     }
   }
   fence_proxy_async_smem();  // the bulk copies read qrow through the async proxy
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int i = 0; i < n; ++i) bulk_store(xq + static_cast<size_t>(rows[i]) * Kp, qrow, Kp);
+    for (int i = 0; i < n; ++i) bulk_store(xq + static_cast<size_t>(rows[i]) * row_bytes, qrow, row_bytes);
   }
   // exponent words: scattered in the MMA scale layout, plain stores
   for (int j = threadIdx.x; j < n * nblk; j += blockDim.x) {

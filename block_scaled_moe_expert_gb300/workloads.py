@@ -19,6 +19,10 @@ used, every tensor is drawn from a seeded generator:
   FP8 -- e4m3 codes with one fp32 scale per 128x128 block, scale = amax/448;
   FP4 -- e2m1 codes packed two per byte (low nibble = even K index) with one
   UE8M0 byte per 1x32 block, exponent n = min{n : amax <= 6 * 2^n}.
+
+``act_fmt`` names the activation format the forward is asked to use ("fp8":
+e4m3 1x128, the pages' rule; "fp4": the FP4 x FP4 variant). It selects the
+computation, not the inputs: the drawn bytes are the same.
 """
 import math
 from dataclasses import dataclass, field
@@ -44,6 +48,7 @@ class Workload:
     skip_frac: float = 0.0
     swiglu_limit: float | None = None
     seed: int = 1000
+    act_fmt: str = "fp8"   # "fp8" | "fp4" (FP4 weights only)
 
     @property
     def S(self):
@@ -67,6 +72,13 @@ WORKLOADS = {
 for _t in (1, 8, 32, 128, 512, 2048):
     WORKLOADS[f"dsv3_decode_fp4_T{_t}"] = _w(f"dsv3_decode_fp4_T{_t}", _t, 7168, 2048, 256, 8, FP4,
                                              "zipf_sigmoid", 1004)
+# The FP4 x FP4 variant (e2m1 activations) on the GPT-OSS and DeepSeek-V3
+# decode shapes: same inputs as their FP8-activation counterparts.
+WORKLOADS["gptoss_fp4xfp4"] = _w("gptoss_fp4xfp4", 8192, 2880, 2880, 128, 4, FP4, "softmax", 1003,
+                                 logit_std=1.5, swiglu_limit=7.0, act_fmt=FP4)
+for _t in (1, 128):
+    WORKLOADS[f"dsv3_decode_fp4xfp4_T{_t}"] = _w(f"dsv3_decode_fp4xfp4_T{_t}", _t, 7168, 2048, 256, 8, FP4,
+                                                 "zipf_sigmoid", 1004, act_fmt=FP4)
 
 
 def scaled(wl: Workload, **changes) -> Workload:

@@ -30,6 +30,15 @@
  *              (weight = code * 2^(byte - 127)).
  *   Activations (hidden and the SwiGLU output) are quantized per 1x128 block
  *   to e4m3 with a power-of-two scale 2^e, e = min{n : amax <= 448 * 2^n}.
+ *   MOE_W_FP4_ACT_FP4: the FP4 x FP4 variant (both GEMM operands e2m1, the
+ *              tensor cores' FP4 block-scaled MMA): MOE_W_FP4 weights, and
+ *              activations quantized per 1x32 block to e2m1 with a UE8M0
+ *              exponent n = min{n : amax <= 6 * 2^n} (round to nearest even,
+ *              sign of zero kept, two codes per byte, low nibble = even
+ *              column). The pages name FP4 x FP4 only as a variant; its
+ *              activation rule here is the microscaling rule of the FP4
+ *              weights. Results differ from MOE_W_FP4 by the coarser
+ *              activation rounding.
  *   SwiGLU: rows [0, I) of w13 are gate, [I, 2I) are up; with a limit L,
  *   gate = min(gate, L) and up = clamp(up, -L, L); act = silu(gate) * up.
  *
@@ -75,8 +84,9 @@ typedef enum {
 } moe_status;
 
 typedef enum {
-  MOE_W_FP8 = 0, /* e4m3 + fp32 128x128 block scales */
-  MOE_W_FP4 = 1  /* e2m1 packed in bytes + UE8M0 1x32 block scales */
+  MOE_W_FP8 = 0,         /* e4m3 + fp32 128x128 block scales */
+  MOE_W_FP4 = 1,         /* e2m1 packed in bytes + UE8M0 1x32 block scales */
+  MOE_W_FP4_ACT_FP4 = 2  /* MOE_W_FP4 weights with e2m1 1x32 activations */
 } moe_wfmt;
 
 /* Sticky flags in the workspace status word (moe_get_device_status). */
@@ -91,7 +101,8 @@ int moe_abi_version(void);
 
 /*
  * Supported shapes: 1 <= E <= 512, 1 <= K <= 32, H and I multiples of 64
- * (multiples of 128 for MOE_W_FP8, whose weight blocks are 128x128),
+ * (multiples of 128 for MOE_W_FP8, whose weight blocks are 128x128; the
+ * FP4 formats take multiples of 64),
  * 128 <= H, I <= 32768. T may be 0 (nothing is enqueued).
  */
 
@@ -121,7 +132,8 @@ size_t moe_workspace_bytes(int fmt, int T_max, int H, int I, int E, int K);
  *   MOE_W_FP8: w13 u8 [E, 2I, H], w13_scale f32 [E, 2I/128, H/128],
  *              w2  u8 [E, H, I],  w2_scale  f32 [E, H/128, I/128];
  *   MOE_W_FP4: w13 u8 [E, 2I, H/2], w13_scale u8 [E, 2I, H/32],
- *              w2  u8 [E, H, I/2],  w2_scale  u8 [E, H, I/32].
+ *              w2  u8 [E, H, I/2],  w2_scale  u8 [E, H, I/32];
+ *   MOE_W_FP4_ACT_FP4: as MOE_W_FP4 (same inputs, same prepared bytes).
  * Outputs (device, caller-owned): w13_prep of moe_prepared_w13_bytes,
  *   w2_prep of moe_prepared_w2_bytes. Their content is opaque.
  * Errors: MOE_ERR_INVALID_ARG / UNSUPPORTED_SHAPE / ALIGNMENT /
@@ -175,6 +187,8 @@ moe_status moe_prepare_weights_transposed(int fmt, int E, int H, int I, const vo
  * T*K <= 32 the whole forward is one cooperative launch of one CTA per SM
  * (GEMM2 work units wait on device counters for the GEMM1 units of their
  * rows), which needs every SM of the device free for the launch.
+ * MOE_W_FP4_ACT_FP4 always runs routing, quantization, GEMM1, GEMM2 and the
+ * combine as five launches (128-row tiles at every batch size).
  */
 moe_status moe_experts_forward(const void* hidden, const int32_t* topk_idx, const float* topk_w, int T, int H,
                                int I, int E, int K, int fmt, const void* w13_prep, const void* w2_prep,
@@ -188,7 +202,8 @@ moe_status moe_experts_forward(const void* hidden, const int32_t* topk_idx, cons
  * 2 after the input quantization, 3 after GEMM1 (+SwiGLU epilogue),
  * 4 after GEMM2, 5 after the combine. `events` points to 6 entries (host
  * memory). Where stages share a kernel the events between them are recorded
- * back to back: routing and quantization for T*K <= 256 (events 1 and 2),
+ * back to back: routing and quantization for T*K <= 256 (events 1 and 2;
+ * not for MOE_W_FP4_ACT_FP4),
  * GEMM2 and the combine for FP4 weights with T*K <= 256 and T*K <= 8E
  * (events 4 and 5), and every stage for FP4 weights with T*K <= 32 and
  * T*K <= 8E, which run as one launch (events 1 to 5 after it). Meant for
@@ -283,13 +298,18 @@ moe_status moe_selftest_wait_timeout(void* workspace, size_t workspace_bytes, vo
  *     128-row m-tiles, [1] number of 32-row chunks, [16 + e] first m-tile
  *     and [16 + E + 1 + e] first chunk of expert e (E+1 entries each), then
  *     the expert owning each m-tile, then the expert owning each chunk;
- *   xq u8 [M, xq_cols] (e4m3 hidden rows in grouped order);
+ *   xq u8 [M, xq_cols] (e4m3 hidden rows in grouped order; for
+ *     MOE_W_FP4_ACT_FP4 u8 [M, xq_cols / 2], e2m1 codes two per byte);
  *   xsf u32 (activation scale words, see below);
- *   act u8 [M, act_cols] (e4m3 SwiGLU output), asf u32 likewise;
+ *   act u8 [M, act_cols] (e4m3 SwiGLU output; for MOE_W_FP4_ACT_FP4
+ *     u8 [M, act_cols / 2] e2m1), asf u32 likewise;
  *   y f32 [M, H] (weighted per-pair outputs).
+ * xq_cols and act_cols count elements (H and I padded to 128).
  * Scale words: for row r and 128-column block b the word sits at index
  *   ((r / 128) * nblk + b) * 128 + 4 * (r % 32) + (r % 128) / 32
- * and holds the UE8M0 byte (e + 127) replicated in all four bytes.
+ * and holds the UE8M0 byte (e + 127) replicated in all four bytes; for
+ * MOE_W_FP4_ACT_FP4 byte j holds the exponent byte (n + 127) of the 1x32
+ * sub-block j of the 128 columns.
  */
 typedef struct {
   size_t total_bytes;
@@ -311,8 +331,8 @@ moe_status moe_query_workspace_layout(int fmt, int T, int H, int I, int E, int K
  * from GEMM1's epilogue, the
  * fp32 SwiGLU values it requantizes -- act = silu(gate) * up after the
  * optional clamp -- so that the requantized bytes (workspace regions act and
- * asf) can be checked bit for bit against the 1x128 rule applied to exactly
- * these values. Row r of the padded grouped layout goes to
+ * asf) can be checked bit for bit against the 1x128 rule (the 1x32 e2m1 rule
+ * for MOE_W_FP4_ACT_FP4) applied to exactly these values. Row r of the padded grouped layout goes to
  * act_f32[r * act_cols + j], j < act_cols (moe_query_workspace_layout;
  * columns j >= I hold 0); padding rows are not written.
  *   act_f32  device fp32, >= row_capacity * act_cols * 4 bytes, 32-byte

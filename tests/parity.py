@@ -44,12 +44,12 @@ def bits_of(hidden):
     return hidden.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def oracle_out(hidden, idx, w, weights, limit, tokens=None):
+def oracle_out(hidden, idx, w, weights, limit, tokens=None, act_fmt="fp8"):
     return OM.experts_forward(bits_of(hidden), idx.cpu().numpy(), w.cpu().numpy(), oracle_weights(weights),
-                              limit, tokens=tokens)
+                              limit, tokens=tokens, act_fmt=act_fmt)
 
 
-def oracle_out_parallel(hidden, idx, w, weights, limit, tokens, threads=None):
+def oracle_out_parallel(hidden, idx, w, weights, limit, tokens, threads=None, act_fmt="fp8"):
     """oracle_out for many tokens of a large workload, expert groups in threads.
 
     The pairs of the selected tokens are split by expert into groups; each
@@ -71,7 +71,7 @@ def oracle_out_parallel(hidden, idx, w, weights, limit, tokens, threads=None):
 
     def run(group):
         masked = np.where(np.isin(ids, group), ids, -1).astype(ids.dtype)
-        return OM.experts_forward(bits, masked, wv, oracle_weights(weights), limit, tokens=tokens)
+        return OM.experts_forward(bits, masked, wv, oracle_weights(weights), limit, tokens=tokens, act_fmt=act_fmt)
 
     out = np.zeros((len(tokens), bits.shape[1]), dtype=np.float64)
     if not groups:
@@ -132,13 +132,19 @@ def assert_close(gpu_bf16, ref, what=""):
     return m
 
 
+def lib_fmt(wl):
+    """The library's format name for a workload (weights + activations)."""
+    return "fp4_act_fp4" if wl.act_fmt == "fp4" else wl.fmt
+
+
 def run_cuda(wl, device="cuda", hidden=None, idx=None, w=None, weights=None, prepared=None):
     hidden = W.make_hidden(wl, device) if hidden is None else hidden
     if idx is None:
         idx, w = W.make_routing(wl, device)
     weights = W.make_weights(wl, device) if weights is None else weights
-    prepared = B.prepare_weights(weights) if prepared is None else prepared
-    ws = torch.empty(B.workspace_bytes(wl.fmt, wl.T, wl.H, wl.I, wl.E, wl.K), dtype=torch.uint8, device=device)
+    prepared = B.prepare_weights(weights, activations=wl.act_fmt) if prepared is None else prepared
+    ws = torch.empty(B.workspace_bytes(prepared.fmt, wl.T, wl.H, wl.I, wl.E, wl.K), dtype=torch.uint8,
+                     device=device)
     out = B.experts_forward(hidden, idx, w, prepared, wl.swiglu_limit, workspace=ws)
     torch.cuda.synchronize()
     return dict(hidden=hidden, idx=idx, w=w, weights=weights, prepared=prepared, ws=ws, out=out)
@@ -159,5 +165,25 @@ def sf_exponents(words_u32, rows, nblk):
     return (w[idx] & 0xFF) - 127
 
 
-__all__ = ["oracle_out", "oracle_out_parallel", "sample_tokens", "compare", "assert_close", "run_cuda", "ws_region", "sf_exponents", "bits_of", "OF",
-           "OM", "W", "B"]
+def sf_exponents_1x32(words_u32, rows, nblk):
+    """FP4 activations: the exponent of every 1x32 block, [rows, 4 * nblk]
+    (byte j of the (row, 128-column block) word is sub-block j)."""
+    w = words_u32.cpu().numpy().astype(np.int64)
+    r = np.arange(rows)[:, None]
+    b = np.arange(nblk)[None, :]
+    idx = ((r // 128) * nblk + b) * 128 + 4 * (r % 32) + (r % 128) // 32
+    words = w[idx]
+    return np.stack([((words >> (8 * j)) & 0xFF) - 127 for j in range(4)], axis=2).reshape(rows, 4 * nblk)
+
+
+def unpack_e2m1(packed_u8, cols):
+    """Packed e2m1 bytes [R, cols / 2] -> 4-bit codes [R, cols] (even column in the low nibble)."""
+    b = np.asarray(packed_u8, dtype=np.uint8)
+    c = np.empty((b.shape[0], 2 * b.shape[1]), dtype=np.uint8)
+    c[:, 0::2] = b & 0xF
+    c[:, 1::2] = b >> 4
+    return c[:, :cols]
+
+
+__all__ = ["oracle_out", "oracle_out_parallel", "sample_tokens", "compare", "assert_close", "run_cuda", "ws_region",
+           "sf_exponents", "sf_exponents_1x32", "unpack_e2m1", "lib_fmt", "bits_of", "OF", "OM", "W", "B"]

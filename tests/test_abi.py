@@ -30,7 +30,8 @@ def test_status_strings_and_version(L):
 
 
 @pytest.mark.parametrize("fmt,E,H,I", [(0, 8, 4096, 14336), (0, 256, 7168, 2048), (1, 128, 2880, 2880),
-                                       (1, 256, 7168, 2048), (0, 8, 256, 128)])
+                                       (1, 256, 7168, 2048), (0, 8, 256, 128), (2, 128, 2880, 2880),
+                                       (2, 256, 7168, 2048)])
 def test_sizes_are_consistent(L, fmt, E, H, I):
     n13 = L.moe_prepared_w13_bytes(fmt, E, H, I)
     n2 = L.moe_prepared_w2_bytes(fmt, E, H, I)
@@ -52,12 +53,18 @@ def test_sizes_are_consistent(L, fmt, E, H, I):
         assert lay.row_capacity >= S and lay.row_capacity % 128 == 0
         assert lay.row_capacity <= S + min(E, S) * 127 + 127
         assert lay.y + 4 * lay.row_capacity * H <= lay.total_bytes
+        assert lay.xq_cols == kp1 and lay.act_cols == kp2
+        # activation rows: a byte per code, or two e2m1 codes per byte (fmt 2)
+        per = 2 if fmt == 2 else 1
+        assert lay.xsf >= lay.xq + lay.row_capacity * kp1 // per
+        assert lay.asf >= lay.act + lay.row_capacity * kp2 // per
         # monotone in T: a workspace sized for T serves every smaller T
         assert L.moe_workspace_bytes(fmt, T, H, I, E, K) >= L.moe_workspace_bytes(fmt, max(T - 1, 0), H, I, E, K)
 
 
 @pytest.mark.parametrize("fmt,E,H,I,K", [(0, 8, 200, 128, 2), (0, 8, 256, 192, 2), (1, 8, 250, 128, 2),
-                                         (2, 8, 256, 128, 2), (0, 0, 256, 128, 2), (0, 513, 256, 128, 2),
+                                         (3, 8, 256, 128, 2), (2, 8, 250, 128, 2), (0, 0, 256, 128, 2),
+                                         (0, 513, 256, 128, 2),
                                          (0, 8, 64, 128, 2)])
 def test_unsupported_shapes_are_refused(L, fmt, E, H, I, K):
     assert L.moe_workspace_bytes(fmt, 16, H, I, E, K) == 0
@@ -114,3 +121,20 @@ def test_python_refusals_without_gpu():
         B.experts_forward(torch.zeros(2, 256), torch.zeros(2, 2, dtype=torch.int32), torch.zeros(2, 2), None)
     with pytest.raises(NotImplementedError):
         B.experts_forward(torch.zeros(2, 256, dtype=torch.bfloat16), None, None, None, activation_scheme="static")
+
+
+def test_fp4_activation_format_shares_the_fp4_weights(L):
+    for E, H, I in [(8, 256, 128), (128, 2880, 2880)]:
+        assert L.moe_prepared_w13_bytes(2, E, H, I) == L.moe_prepared_w13_bytes(1, E, H, I) > 0
+        assert L.moe_prepared_w2_bytes(2, E, H, I) == L.moe_prepared_w2_bytes(1, E, H, I) > 0
+        # the e2m1 activation rows take half the bytes of the e4m3 ones
+        assert L.moe_workspace_bytes(2, 4096, H, I, E, 4) < L.moe_workspace_bytes(1, 4096, H, I, E, 4)
+
+
+def test_python_refuses_fp4_activations_with_fp8_weights():
+    with pytest.raises(ValueError):
+        B.prepare_weights(dict(fmt="fp8", E=1, H=128, I=128, w13=None, w13_scale=None, w2=None, w2_scale=None),
+                          activations="fp4")
+    with pytest.raises(ValueError):
+        B.prepare_weights(dict(fmt="fp4", E=1, H=128, I=128, w13=None, w13_scale=None, w2=None, w2_scale=None),
+                          activations="int8")

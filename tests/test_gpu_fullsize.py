@@ -19,7 +19,7 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 W = P.W
 NAMES = ["mixtral_prefill_fp8", "dsv3_decode_fp8", "dsv3_prefill_fp8", "gptoss_fp8xfp4", "dsv3_decode_fp4_T1",
          "dsv3_decode_fp4_T8", "dsv3_decode_fp4_T32", "dsv3_decode_fp4_T128", "dsv3_decode_fp4_T512",
-         "dsv3_decode_fp4_T2048"]
+         "dsv3_decode_fp4_T2048", "gptoss_fp4xfp4", "dsv3_decode_fp4xfp4_T1", "dsv3_decode_fp4xfp4_T128"]
 MIN_SAMPLE = 64
 
 
@@ -32,7 +32,7 @@ def test_full_size_workload(name):
     assert P.B.device_status(r["ws"]) == 0
 
     # routing of the whole batch against the oracle
-    L = P.B.workspace_layout(wl.fmt, wl.T, wl.H, wl.I, wl.E, wl.K)
+    L = P.B.workspace_layout(P.lib_fmt(wl), wl.T, wl.H, wl.I, wl.E, wl.K)
     ref_route = route(r["idx"].cpu().numpy(), wl.E, L.row_align)
     inv = P.ws_region(r["ws"], L, "inv", torch.int32, wl.S).cpu().numpy()
     assert (inv == ref_route["inv"]).all()
@@ -48,6 +48,7 @@ def test_full_size_workload(name):
     touched = set(np.unique(r["idx"].cpu().numpy()).tolist()) - {-1}
     assert set(np.unique(sel).tolist()) - {-1} == touched
     assert len(toks) >= min(MIN_SAMPLE, wl.T)
-    ref = P.oracle_out_parallel(r["hidden"], r["idx"], r["w"], r["weights"], wl.swiglu_limit, toks)
+    ref = P.oracle_out_parallel(r["hidden"], r["idx"], r["w"], r["weights"], wl.swiglu_limit, toks,
+                                act_fmt=wl.act_fmt)
     m = P.assert_close(out[toks], ref, name)
     print(name, len(toks), "tokens,", len(touched), "experts", m)
