@@ -382,9 +382,9 @@ moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, cons
       if (!mark(i)) return MOE_ERR_CUDA;
     return MOE_OK;
   }
-  if (L.S <= kFusedRouteQuantSlots && !mx) {
+  if (L.S <= kFusedRouteQuantSlots) {
     // One launch for both (the quant stage then has zero length).
-    if (launch_route_quant_small(topk_idx, hidden, topk_w, T, H, E, K, L, ws, out, st) != cudaSuccess || !mark(1) ||
+    if (launch_route_quant_small(fmt, topk_idx, hidden, topk_w, T, H, E, K, L, ws, out, st) != cudaSuccess || !mark(1) ||
         !mark(2))
       return MOE_ERR_CUDA;
   } else {

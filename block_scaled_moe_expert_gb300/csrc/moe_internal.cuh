@@ -114,8 +114,9 @@ cudaError_t launch_quant(int fmt, const void* hidden, const float* topk_w, int T
 // counts, zeroed arrival counters, and the +0 output rows of tokens whose
 // slots are all skipped.
 constexpr int kFusedRouteQuantSlots = 256;
-cudaError_t launch_route_quant_small(const int32_t* topk_idx, const void* hidden, const float* topk_w, int T, int H,
-                                     int E, int K, const WsLayout& L, uint8_t* ws, void* out, cudaStream_t st);
+cudaError_t launch_route_quant_small(int fmt, const int32_t* topk_idx, const void* hidden, const float* topk_w, int T,
+                                     int H, int E, int K, const WsLayout& L, uint8_t* ws, void* out,
+                                     cudaStream_t st);
 // The top-k combine fused into GEMM2's epilogue: decode mode with the fused
 // routing + quantization front end. At larger decode batches the separate
 // combine kernel is faster (the epilogue's combines then hold up the

@@ -52,13 +52,14 @@ quant_permute_kernel(const __nv_bfloat16* __restrict__ hidden, const float* __re
 // ---------------------------------------------------------------------------
 // Small batches (T * K <= kFusedRouteQuantSlots): routing and quantization in
 // one launch, one CTA per token (route_quant.cuh).
+template <bool kFp4>
 __global__ void __launch_bounds__(kQuantWarps * 32) route_quant_small_kernel(const RqArgs a) {
   __shared__ RqSmem<kQuantWarps> sm;
   pdl_wait();
   pdl_launch_dependents();
   route_small_in_smem<kQuantWarps>(sm, a);
   if (blockIdx.x == 0) write_routing<kQuantWarps>(sm, a);
-  quantize_tokens<kQuantWarps, false>(sm, a, blockIdx.x, gridDim.x);
+  quantize_tokens<kQuantWarps, false, kFp4>(sm, a, blockIdx.x, gridDim.x);
 }
 
 }  // namespace
@@ -106,13 +107,14 @@ RqArgs make_rq_args(const int32_t* topk_idx, const void* hidden, const float* to
   return a;
 }
 
-cudaError_t launch_route_quant_small(const int32_t* topk_idx, const void* hidden, const float* topk_w, int T, int H,
-                                     int E, int K,
-                                     const WsLayout& L, uint8_t* ws, void* out, cudaStream_t st) {
+cudaError_t launch_route_quant_small(int fmt, const int32_t* topk_idx, const void* hidden, const float* topk_w, int T,
+                                     int H, int E, int K, const WsLayout& L, uint8_t* ws, void* out,
+                                     cudaStream_t st) {
   // The first kernel of the forward is an ordinary launch: it follows
   // whatever the caller queued on the stream.
-  return launch_kernel(false, route_quant_small_kernel, T, kQuantWarps * 32, 0, st,
-                       make_rq_args(topk_idx, hidden, topk_w, T, H, E, K, L, ws, out));
+  return launch_kernel(false,
+                       fmt == MOE_W_FP4_ACT_FP4 ? route_quant_small_kernel<true> : route_quant_small_kernel<false>, T,
+                       kQuantWarps * 32, 0, st, make_rq_args(topk_idx, hidden, topk_w, T, H, E, K, L, ws, out));
 }
 
 }  // namespace bsmoe
