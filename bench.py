@@ -167,11 +167,11 @@ def launches_per_forward(wl):
     kernel up to 8192 slots or histogram + scan + scatter, then the
     quantization kernel), GEMM1, GEMM2, and the combine (inside GEMM2 for FP4
     weights with at most 8 pairs per expert and at most 256 slots). With FP4
-    activations the GEMMs always run 128-row tiles (no decode mode, no single
-    launch, the separate combine)."""
+    activations routing and quantization are separate kernels at every size
+    and the GEMMs run 128-row tiles (no decode mode, no single launch)."""
     S = wl.T * wl.K
     if wl.act_fmt == "fp4":
-        return (1 if S <= 256 else (2 if S <= 8192 else 4)) + 2 + 1
+        return (2 if S <= 8192 else 4) + 2 + 1
     if wl.fmt == "fp4" and S <= 8 * wl.E and S <= 32:
         return 1  # the single-launch decode forward
     front = 1 if S <= 256 else (2 if S <= 8192 else 4)

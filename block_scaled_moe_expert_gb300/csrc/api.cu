@@ -382,7 +382,9 @@ moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, cons
       if (!mark(i)) return MOE_ERR_CUDA;
     return MOE_OK;
   }
-  if (L.S <= kFusedRouteQuantSlots) {
+  // FP4 activations keep the two kernels at every size: at one token of the
+  // DeepSeek-V3 shape the fused kernel made the step 0.064 ms against 0.061.
+  if (L.S <= kFusedRouteQuantSlots && !mx) {
     // One launch for both (the quant stage then has zero length).
     if (launch_route_quant_small(fmt, topk_idx, hidden, topk_w, T, H, E, K, L, ws, out, st) != cudaSuccess || !mark(1) ||
         !mark(2))

@@ -54,14 +54,14 @@ def test_launch_count_follows_the_library_thresholds():
     assert bench.launches_per_forward(wl(fused, 1, E - 1, "fp4")) == 1 + 2 + 1  # not decode mode
     assert bench.launches_per_forward(wl(fused + 1, 1, 4 * E, "fp4")) == 2 + 2 + 1  # decode, separate combine
     # every named workload is one of these cases
-    # FP4 activations: tile mode and the separate combine at every size
-    assert bench.launches_per_forward(W.scaled(wl(one, 1, E, "fp4"), act_fmt="fp4")) == 1 + 2 + 1
+    # FP4 activations: routing and quantization apart, tile mode, separate combine
+    assert bench.launches_per_forward(W.scaled(wl(one, 1, E, "fp4"), act_fmt="fp4")) == 2 + 2 + 1
     assert bench.launches_per_forward(W.scaled(wl(fused + 1, 1, E, "fp4"), act_fmt="fp4")) == 2 + 2 + 1
     assert bench.launches_per_forward(W.scaled(wl(single + 1, 1, E, "fp4"), act_fmt="fp4")) == 4 + 2 + 1
     for name, w in W.WORKLOADS.items():
         S = w.T * w.K
         if w.act_fmt == "fp4":
-            assert bench.launches_per_forward(w) == (1 if S <= fused else (2 if S <= single else 4)) + 2 + 1, name
+            assert bench.launches_per_forward(w) == (2 if S <= single else 4) + 2 + 1, name
             continue
         front = 1 if S <= fused else (2 if S <= single else 4)
         decode_fused = w.fmt == "fp4" and S <= per_expert * w.E and S <= fused

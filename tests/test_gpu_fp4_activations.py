@@ -123,3 +123,88 @@ def test_fp4_activation_forward_replays_from_a_cuda_graph():
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int16), r["out"].view(torch.int16))
+
+
+def _sweep_hidden_fp4():
+    """Every finite bf16 value (shuffled, so the blocks' amax vary), then
+    blocks holding every e2m1 rounding tie at several scales next to their
+    block amax 6 * 2^n."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    v = OF.bf16_bits_to_f64(bits)
+    fin = bits[np.isfinite(v)]
+    rng = np.random.default_rng(1)
+    H = 1024
+    shuffled = fin[rng.permutation(fin.size)]
+    rows = [np.concatenate([shuffled, np.zeros((-shuffled.size) % H, np.uint16)]).reshape(-1, H)]
+    pos = OF.E2M1_TABLE[:8]
+    mids = (pos[1:] + pos[:-1]) / 2
+    vals, exact = [], []
+    for n in range(-20, 21, 3):
+        blk = np.zeros(32)
+        blk[0] = 6.0 * 2.0 ** n
+        blk[1:1 + mids.size] = mids * 2.0 ** n
+        blk[1 + mids.size:1 + 2 * mids.size] = -mids * 2.0 ** n
+        ex = np.ones(32, bool)
+        blk[1 + 2 * mids.size] = -0.1 * 2.0 ** n  # rounds to -0 (not exact in bf16)
+        ex[1 + 2 * mids.size] = False
+        vals.append(blk)
+        exact.append(ex)
+    tie, exact = np.concatenate(vals), np.concatenate(exact)
+    tie_bits = (tie.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    assert (OF.bf16_bits_to_f64(tie_bits)[exact] == tie[exact]).all()
+    # the exponent clamps: a block of subnormal bf16 values (n = -127) and one
+    # at the top of the bf16 range (n = 126)
+    tiny = np.arange(1, 33, dtype=np.uint16)
+    huge = np.arange(0x7F7F, 0x7F7F - 32, -1, dtype=np.uint16) | np.tile(np.array([0, 0x8000], np.uint16), 16)
+    tie_bits = np.concatenate([tie_bits, tiny, huge])
+    tie_bits = np.concatenate([tie_bits, np.zeros((-tie_bits.size) % H, np.uint16)]).reshape(-1, H)
+    rows.append(tie_bits)
+    return np.concatenate(rows)
+
+
+def test_fp4_quantizer_exhaustive_bf16_sweep():
+    hb = _sweep_hidden_fp4()
+    T, H = hb.shape
+    wl = W.Workload("sweep_fp4", T, H, 128, 2, 1, "fp4", "softmax", seed=78, act_fmt="fp4")
+    hidden = torch.from_numpy(hb.view(np.int16)).view(torch.bfloat16).cuda()
+    idx = (torch.arange(T, dtype=torch.int32, device="cuda") % 2).view(T, 1).contiguous()
+    w = torch.ones(T, 1, dtype=torch.float32, device="cuda")
+    r = P.run_cuda(wl, hidden=hidden, idx=idx, w=w)
+    L = _layout(wl)
+    inv = P.ws_region(r["ws"], L, "inv", torch.int32, T).cpu().numpy()
+    packed = P.ws_region(r["ws"], L, "xq", torch.uint8, L.row_capacity * L.xq_cols // 2)
+    codes = P.unpack_e2m1(packed.view(L.row_capacity, L.xq_cols // 2).cpu().numpy()[inv], L.xq_cols)
+    exps = P.sf_exponents_1x32(P.ws_region(r["ws"], L, "xsf", torch.int32, L.row_capacity * L.x_blocks),
+                               L.row_capacity, L.x_blocks)[inv]
+    want_c, want_e = P.OM.quantize_hidden(hb, act_fmt="fp4")
+    assert np.array_equal(exps, want_e), np.argwhere(exps != want_e)[:8]
+    bad = np.argwhere(codes != want_c)
+    assert bad.size == 0, [(int(t), int(c), int(codes[t, c]), int(want_c[t, c]), int(hb[t, c])) for t, c in bad[:8]]
+    # the sweep reaches every code, ties and negative zero included, and both exponent ends
+    assert set(np.unique(want_c).tolist()) == set(range(16))
+    assert want_e.min() == -127 and want_e.max() == 126
+
+
+def _random_configs(n=8, seed=20241):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        H = int(rng.integers(2, 9)) * 64
+        I = int(rng.integers(2, 9)) * 64
+        E = int(rng.choice([4, 8, 16, 33, 64]))
+        K = int(min(E, rng.choice([1, 2, 4, 8])))
+        T = int(rng.choice([1, 3, 17, 64, 150, 300]))
+        router = str(rng.choice(["softmax", "zipf_sigmoid"]))
+        skip = float(rng.choice([0.0, 0.1]))
+        limit = None if rng.random() < 0.5 else float(np.round(rng.uniform(0.1, 5.0), 3))
+        out.append(W.Workload(f"mxsweep{i}_T{T}_H{H}_I{I}_E{E}_K{K}", T, H, I, E, K, "fp4", router,
+                              seed=4000 + i, skip_frac=skip, swiglu_limit=limit, act_fmt="fp4"))
+    return out
+
+
+@pytest.mark.parametrize("wl", _random_configs(), ids=lambda w: w.name)
+def test_fp4_activation_random_configuration_matches_oracle(wl):
+    r = P.run_cuda(wl)
+    ref = P.oracle_out(r["hidden"], r["idx"], r["w"], r["weights"], wl.swiglu_limit, act_fmt="fp4")
+    P.assert_close(r["out"], ref, wl.name)
+    assert P.B.device_status(r["ws"]) == 0
