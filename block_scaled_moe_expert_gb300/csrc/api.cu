@@ -382,9 +382,12 @@ moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, cons
       if (!mark(i)) return MOE_ERR_CUDA;
     return MOE_OK;
   }
-  // FP4 activations keep the two kernels at every size: at one token of the
-  // DeepSeek-V3 shape the fused kernel made the step 0.064 ms against 0.061.
-  if (L.S <= kFusedRouteQuantSlots && !mx) {
+  // Routing and quantization in one launch only where that kernel also sets
+  // up the combine in GEMM2's epilogue (FP4 decode batches of at most 256
+  // slots). Elsewhere the two kernels are faster (DeepSeek-V3 shape, same
+  // box: FP8 weights T=16 0.453 against 0.462 ms, T=32 0.682 against 0.694;
+  // FP4 activations T=1 0.061 against 0.064).
+  if (fuse_combine) {
     // One launch for both (the quant stage then has zero length).
     if (launch_route_quant_small(fmt, topk_idx, hidden, topk_w, T, H, E, K, L, ws, out, st) != cudaSuccess || !mark(1) ||
         !mark(2))

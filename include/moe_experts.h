@@ -202,8 +202,8 @@ moe_status moe_experts_forward(const void* hidden, const int32_t* topk_idx, cons
  * 2 after the input quantization, 3 after GEMM1 (+SwiGLU epilogue),
  * 4 after GEMM2, 5 after the combine. `events` points to 6 entries (host
  * memory). Where stages share a kernel the events between them are recorded
- * back to back: routing and quantization for T*K <= 256 (events 1 and 2;
- * not for MOE_W_FP4_ACT_FP4),
+ * back to back: routing and quantization for FP4 weights with T*K <= 256
+ * and T*K <= 8E (events 1 and 2),
  * GEMM2 and the combine for FP4 weights with T*K <= 256 and T*K <= 8E
  * (events 4 and 5), and every stage for FP4 weights with T*K <= 32 and
  * T*K <= 8E, which run as one launch (events 1 to 5 after it). Meant for
