@@ -162,19 +162,17 @@ def weight_bytes_per_expert(wl, which):
 
 def launches_per_forward(wl):
     """Kernels one forward launches: one for FP4 weights with at most 8 pairs
-    per expert and at most 32 slots (the single-launch forward); for FP4
-    weights with at most 8 pairs per expert and at most 256 slots, one fused
-    routing + quantization kernel, GEMM1 and GEMM2 (with the combine in its
-    epilogue); otherwise the routing (one kernel up to 8192 slots, else
-    histogram + scan + scatter), the quantization kernel, GEMM1, GEMM2 and the
-    combine. FP4 activations never use the decode mode."""
+    per expert and at most 32 slots (the single-launch forward); otherwise the
+    routing (one kernel up to 8192 slots, else histogram + scan + scatter),
+    the quantization kernel, GEMM1, GEMM2 and the combine (inside GEMM2 for
+    FP4 weights with at most 8 pairs per expert and at most 256 slots). FP4
+    activations never use the decode mode."""
     S = wl.T * wl.K
     decode = wl.fmt == "fp4" and wl.act_fmt == "fp8" and S <= 8 * wl.E
     if decode and S <= 32:
         return 1  # the single-launch decode forward
-    if decode and S <= 256:
-        return 1 + 2  # fused front end, GEMM1, GEMM2 with the combine
-    return (2 if S <= 8192 else 4) + 2 + 1
+    combine = 0 if (decode and S <= 256) else 1
+    return (2 if S <= 8192 else 4) + 2 + combine
 
 
 def routing_stats(idx_cpu, E):

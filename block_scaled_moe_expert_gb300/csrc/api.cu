@@ -382,20 +382,12 @@ moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, cons
       if (!mark(i)) return MOE_ERR_CUDA;
     return MOE_OK;
   }
-  // Routing and quantization in one launch only where that kernel also sets
-  // up the combine in GEMM2's epilogue (FP4 decode batches of at most 256
-  // slots). Elsewhere the two kernels are faster (DeepSeek-V3 shape, same
-  // box: FP8 weights T=16 0.453 against 0.462 ms, T=32 0.682 against 0.694;
-  // FP4 activations T=1 0.061 against 0.064).
-  if (fuse_combine) {
-    // One launch for both (the quant stage then has zero length).
-    if (launch_route_quant_small(fmt, topk_idx, hidden, topk_w, T, H, E, K, L, ws, out, st) != cudaSuccess || !mark(1) ||
-        !mark(2))
-      return MOE_ERR_CUDA;
-  } else {
-    if (launch_route(topk_idx, L.S, E, L, ws, st) != cudaSuccess || !mark(1)) return MOE_ERR_CUDA;
-    if (launch_quant(fmt, hidden, topk_w, T, H, K, L, ws, st) != cudaSuccess || !mark(2)) return MOE_ERR_CUDA;
-  }
+  // Routing and quantization as two kernels (one kernel for both, which the
+  // single launch runs as device code, was slower at every batch size it was
+  // measured on: the quantization kernel's dependent launch hides the routing
+  // kernel's tail, and each CTA of the fused kernel recomputed the routing).
+  if (launch_route(topk_idx, L.S, E, L, ws, st) != cudaSuccess || !mark(1)) return MOE_ERR_CUDA;
+  if (launch_quant(fmt, hidden, topk_w, T, H, K, L, ws, out, st) != cudaSuccess || !mark(2)) return MOE_ERR_CUDA;
 
   if (launch_gemm(fmt, true, decode, ta1, tb1, a1, d.sms, st) != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;
 

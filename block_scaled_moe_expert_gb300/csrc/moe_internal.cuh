@@ -107,22 +107,19 @@ cudaError_t launch_kernel(bool dependent, void (*kern)(KArgs...), dim3 grid, dim
 
 // ---------------------------------------------------------------- launches
 cudaError_t launch_route(const int32_t* topk_idx, int S, int E, const WsLayout& L, uint8_t* ws, cudaStream_t st);
+// With the combine in GEMM2's epilogue (fused_combine) the quantization
+// kernel also sets that up: per-token valid-slot counts, zeroed arrival
+// counters, and the +0 output rows of tokens whose slots are all skipped.
 cudaError_t launch_quant(int fmt, const void* hidden, const float* topk_w, int T, int H, int K, const WsLayout& L,
-                         uint8_t* ws, cudaStream_t st);
-// Routing + quantization in one launch, for S = T * K <= kFusedRouteQuantSlots.
-// With the fused combine (below) it also sets that up: per-token valid-slot
-// counts, zeroed arrival counters, and the +0 output rows of tokens whose
-// slots are all skipped.
-constexpr int kFusedRouteQuantSlots = 256;
-cudaError_t launch_route_quant_small(int fmt, const int32_t* topk_idx, const void* hidden, const float* topk_w, int T,
-                                     int H, int E, int K, const WsLayout& L, uint8_t* ws, void* out,
-                                     cudaStream_t st);
-// The top-k combine fused into GEMM2's epilogue: decode mode with the fused
-// routing + quantization front end. At larger decode batches the separate
-// combine kernel is faster (the epilogue's combines then hold up the
-// accumulator hand-back).
+                         uint8_t* ws, void* out, cudaStream_t st);
+// The top-k combine fused into GEMM2's epilogue: decode batches of at most
+// kFusedCombineSlots slots. At larger decode batches the separate combine
+// kernel is faster (the epilogue's combines then hold up the accumulator
+// hand-back). The small-batch routing + quantization device code of the
+// single-launch forward is sized for the same batches.
+constexpr int kFusedCombineSlots = 256;
 inline bool fused_combine(int fmt, long long S, int E) {
-  return decode_mode(fmt, S, E) && S <= kFusedRouteQuantSlots;
+  return decode_mode(fmt, S, E) && S <= kFusedCombineSlots;
 }
 // The whole forward as one cooperative launch (routing + quantization, then
 // the GEMM1 and GEMM2 units of one work list, GEMM2 units waiting on device

@@ -1,5 +1,6 @@
-// Dynamic 1x128 activation quantization fused with the padded permute, and
-// the small-batch kernel that routes and quantizes in one launch.
+// Dynamic activation quantization fused with the padded permute, and the
+// host-side arguments of the small-batch routing + quantization device code
+// that the single-launch decode forward runs.
 //
 // The grouped experts dispatch quantizes activations dynamically per block
 // (error page "grouped_mm experts dispatch does not support
@@ -19,12 +20,15 @@ constexpr int kQuantWarps = 8;
 
 // One CTA per token: gathers the token's valid slots from inv (in ascending
 // k) and quantizes the row into each of their padded rows (kFp4: the e2m1
-// 1x32 rule of the FP4-activation variant).
+// 1x32 rule of the FP4-activation variant). With the combine in GEMM2's
+// epilogue (comb_cnt non-null) it also sets up the token's arrival counters
+// and, for a token whose slots are all skipped, its +0 output row.
 template <bool kFp4>
 __global__ void __launch_bounds__(kQuantWarps * 32)
 quant_permute_kernel(const __nv_bfloat16* __restrict__ hidden, const float* __restrict__ topk_w, int H, int K, int Kp,
                      const int32_t* __restrict__ inv, uint8_t* __restrict__ xq, uint32_t* __restrict__ xsf,
-                     float* __restrict__ row_w) {
+                     float* __restrict__ row_w, int32_t* __restrict__ comb_cnt, int comb_stride,
+                     __nv_bfloat16* __restrict__ out) {
   const int t = blockIdx.x;
   __shared__ int rows[kMaxTopK];
   __shared__ int nrows;
@@ -44,34 +48,24 @@ quant_permute_kernel(const __nv_bfloat16* __restrict__ hidden, const float* __re
     nrows = n;
   }
   __syncthreads();
+  if (comb_cnt != nullptr) setup_combine(t, nrows, comb_cnt, comb_stride, out, H);
   if (nrows == 0) return;
   quantize_token<kQuantWarps, false, kFp4>(hidden + static_cast<size_t>(t) * H, H, Kp, rows, nrows, xq, xsf, qrow,
                                            qsf);
 }
 
-// ---------------------------------------------------------------------------
-// Small batches (T * K <= kFusedRouteQuantSlots): routing and quantization in
-// one launch, one CTA per token (route_quant.cuh).
-template <bool kFp4>
-__global__ void __launch_bounds__(kQuantWarps * 32) route_quant_small_kernel(const RqArgs a) {
-  __shared__ RqSmem<kQuantWarps> sm;
-  pdl_wait();
-  pdl_launch_dependents();
-  route_small_in_smem<kQuantWarps>(sm, a);
-  if (blockIdx.x == 0) write_routing<kQuantWarps>(sm, a);
-  quantize_tokens<kQuantWarps, false, kFp4>(sm, a, blockIdx.x, gridDim.x);
-}
-
 }  // namespace
 
 cudaError_t launch_quant(int fmt, const void* hidden, const float* topk_w, int T, int H, int K, const WsLayout& L,
-                         uint8_t* ws, cudaStream_t st) {
+                         uint8_t* ws, void* out, cudaStream_t st) {
   const moe_workspace_layout& p = L.pub;
   return launch_kernel(true, fmt == MOE_W_FP4_ACT_FP4 ? quant_permute_kernel<true> : quant_permute_kernel<false>, T,
                        kQuantWarps * 32, 0, st,
                        reinterpret_cast<const __nv_bfloat16*>(hidden), topk_w, H, K, p.xq_cols,
                        reinterpret_cast<const int32_t*>(ws + p.inv), ws + p.xq, reinterpret_cast<uint32_t*>(ws + p.xsf),
-                       reinterpret_cast<float*>(ws + L.row_w));
+                       reinterpret_cast<float*>(ws + L.row_w),
+                       L.combine_cnt ? reinterpret_cast<int32_t*>(ws + L.combine_cnt) : nullptr, L.combine_stride,
+                       reinterpret_cast<__nv_bfloat16*>(out));
 }
 
 RqArgs make_rq_args(const int32_t* topk_idx, const void* hidden, const float* topk_w, int T, int H, int E, int K,
@@ -105,16 +99,6 @@ RqArgs make_rq_args(const int32_t* topk_idx, const void* hidden, const float* to
   a.ready = L.chunk_ready ? reinterpret_cast<int32_t*>(ws + L.chunk_ready) : nullptr;
   a.ready_n = L.M / kChunkRows;
   return a;
-}
-
-cudaError_t launch_route_quant_small(int fmt, const int32_t* topk_idx, const void* hidden, const float* topk_w, int T,
-                                     int H, int E, int K, const WsLayout& L, uint8_t* ws, void* out,
-                                     cudaStream_t st) {
-  // The first kernel of the forward is an ordinary launch: it follows
-  // whatever the caller queued on the stream.
-  return launch_kernel(false,
-                       fmt == MOE_W_FP4_ACT_FP4 ? route_quant_small_kernel<true> : route_quant_small_kernel<false>, T,
-                       kQuantWarps * 32, 0, st, make_rq_args(topk_idx, hidden, topk_w, T, H, E, K, L, ws, out));
 }
 
 }  // namespace bsmoe

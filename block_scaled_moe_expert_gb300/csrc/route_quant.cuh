@@ -1,6 +1,7 @@
-// Routing + dynamic 1x128 activation quantization for small batches
-// (T * K <= kFusedRouteQuantSlots), as device code shared by the standalone
-// route+quant kernel and the single-launch decode forward.
+// Routing + dynamic 1x128 activation quantization of a small batch in one
+// kernel, as device code of the single-launch decode forward (T * K <= 32;
+// sized for kFusedCombineSlots), and the per-token quantization shared with
+// the separate quantization kernel.
 //
 // Routing follows fp8_grouped_mm_experts_forward (source excerpt on the error
 // page "grouped_mm experts dispatch does not support
@@ -191,8 +192,8 @@ struct RqArgs {
 // Shared memory of the small-batch routing + quantization.
 template <int kNW>
 struct RqSmem {
-  int key[kFusedRouteQuantSlots];
-  int rank[kFusedRouteQuantSlots];
+  int key[kFusedCombineSlots];
+  int rank[kFusedCombineSlots];
   int cnt[kMaxExperts + 1];
   int off[kMaxExperts + 1];
   int pad[kMaxExperts + 1];
@@ -334,9 +335,8 @@ __device__ __forceinline__ void write_routing(RqSmem<kNW>& sm, const RqArgs& a) 
 }
 
 // Tokens t0, t0 + stride, ... : the valid slots' padded rows (ascending k),
-// the fused-combine setup, and the quantization into those rows (kFp4: the
-// e2m1 1x32 rule of the FP4-activation variant).
-template <int kNW, bool kComplete, bool kFp4 = false>
+// the fused-combine setup, and the quantization into those rows.
+template <int kNW, bool kComplete>
 __device__ __forceinline__ void quantize_tokens(RqSmem<kNW>& sm, const RqArgs& a, int t0, int stride) {
   for (int t = t0; t < a.T; t += stride) {
     if (threadIdx.x == 0) {
@@ -355,8 +355,8 @@ __device__ __forceinline__ void quantize_tokens(RqSmem<kNW>& sm, const RqArgs& a
     const int n = sm.nrows;
     if (a.comb_cnt != nullptr) setup_combine(t, n, a.comb_cnt, a.comb_stride, a.out, a.H);
     if (n > 0)
-      quantize_token<kNW, kComplete, kFp4>(a.hidden + static_cast<size_t>(t) * a.H, a.H, a.Kp, sm.rows, n, a.xq, a.xsf,
-                                           sm.qrow, sm.qsf);
+      quantize_token<kNW, kComplete>(a.hidden + static_cast<size_t>(t) * a.H, a.H, a.Kp, sm.rows, n, a.xq, a.xsf,
+                                     sm.qrow, sm.qsf);
     __syncthreads();  // rows / nrows are rewritten for the next token
   }
 }

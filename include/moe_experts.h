@@ -182,13 +182,14 @@ moe_status moe_prepare_weights_transposed(int fmt, int E, int H, int I, const vo
  * Asynchronous; the workspace must not be used by another call until this
  * one has finished on `stream`.
  *
- * Launches: routing + quantization, GEMM1, GEMM2 and the combine; for FP4
+ * Launches: routing, quantization, GEMM1, GEMM2 and the combine (inside
+ * GEMM2 for FP4 weights with T*K <= 256 and T*K <= 8E); for FP4
  * weights with T*K <= 8E (the weight-streaming decode batches) and
  * T*K <= 32 the whole forward is one cooperative launch of one CTA per SM
  * (GEMM2 work units wait on device counters for the GEMM1 units of their
  * rows), which needs every SM of the device free for the launch.
- * MOE_W_FP4_ACT_FP4 runs routing, quantization, GEMM1, GEMM2 and the
- * combine as separate launches, with 128-row tiles at every batch size.
+ * MOE_W_FP4_ACT_FP4 runs the five launches with 128-row tiles at every
+ * batch size.
  */
 moe_status moe_experts_forward(const void* hidden, const int32_t* topk_idx, const float* topk_w, int T, int H,
                                int I, int E, int K, int fmt, const void* w13_prep, const void* w2_prep,
@@ -202,10 +203,8 @@ moe_status moe_experts_forward(const void* hidden, const int32_t* topk_idx, cons
  * 2 after the input quantization, 3 after GEMM1 (+SwiGLU epilogue),
  * 4 after GEMM2, 5 after the combine. `events` points to 6 entries (host
  * memory). Where stages share a kernel the events between them are recorded
- * back to back: routing and quantization for FP4 weights with T*K <= 256
- * and T*K <= 8E (events 1 and 2),
- * GEMM2 and the combine for FP4 weights with T*K <= 256 and T*K <= 8E
- * (events 4 and 5), and every stage for FP4 weights with T*K <= 32 and
+ * back to back: GEMM2 and the combine for FP4 weights with T*K <= 256 and
+ * T*K <= 8E (events 4 and 5), and every stage for FP4 weights with T*K <= 32 and
  * T*K <= 8E, which run as one launch (events 1 to 5 after it). Meant for
  * measuring the stages; errors as moe_experts_forward.
  */

@@ -29,7 +29,7 @@ def _const(name, fname):
 
 
 def test_launch_count_follows_the_library_thresholds():
-    fused = _const("kFusedRouteQuantSlots", "moe_internal.cuh")
+    fused = _const("kFusedCombineSlots", "moe_internal.cuh")
     per_expert = _const("kDecodePairsPerExpert", "moe_internal.cuh")
     single = _const("kSingleCtaSlots", "route.cu")
 
@@ -38,32 +38,31 @@ def test_launch_count_follows_the_library_thresholds():
 
     # routing (one kernel, or histogram + scan + scatter) + quantization
     assert bench.launches_per_forward(wl(fused, 1, 8, "fp8")) == 2 + 2 + 1
-    assert bench.launches_per_forward(wl(fused + 1, 1, 8, "fp8")) == 2 + 2 + 1
     assert bench.launches_per_forward(wl(single, 1, 8, "fp8")) == 2 + 2 + 1
     assert bench.launches_per_forward(wl(single + 1, 1, 8, "fp8")) == 4 + 2 + 1
     # FP4 decode mode (at most per_expert pairs per expert) with at most
-    # `fused` slots: one routing + quantization kernel and the combine inside
-    # GEMM2; with at most `one` slots the whole forward is one launch
+    # `fused` slots: the combine runs inside GEMM2; with at most `one` slots
+    # the whole forward is one launch
     one = _const("kSingleLaunchSlots", "moe_internal.cuh")
     E = fused // per_expert
-    assert bench.launches_per_forward(wl(fused, 1, E, "fp4")) == 1 + 2
+    assert bench.launches_per_forward(wl(fused, 1, E, "fp4")) == 2 + 2
     assert bench.launches_per_forward(wl(one, 1, E, "fp4")) == 1
-    assert bench.launches_per_forward(wl(one + 1, 1, E, "fp4")) == 1 + 2
+    assert bench.launches_per_forward(wl(one + 1, 1, E, "fp4")) == 2 + 2
     assert bench.launches_per_forward(wl(fused, 1, E, "fp8")) == 2 + 2 + 1
     assert bench.launches_per_forward(wl(fused, 1, E - 1, "fp4")) == 2 + 2 + 1  # not decode mode
     assert bench.launches_per_forward(wl(fused + 1, 1, 4 * E, "fp4")) == 2 + 2 + 1  # decode, separate combine
-    # FP4 activations: routing and quantization apart, tile mode, separate combine
+    # FP4 activations: tile mode, separate combine
     assert bench.launches_per_forward(W.scaled(wl(one, 1, E, "fp4"), act_fmt="fp4")) == 2 + 2 + 1
-    assert bench.launches_per_forward(W.scaled(wl(fused + 1, 1, E, "fp4"), act_fmt="fp4")) == 2 + 2 + 1
     assert bench.launches_per_forward(W.scaled(wl(single + 1, 1, E, "fp4"), act_fmt="fp4")) == 4 + 2 + 1
     # every named workload is one of these cases
     for name, w in W.WORKLOADS.items():
         S = w.T * w.K
-        decode_fused = w.fmt == "fp4" and w.act_fmt == "fp8" and S <= per_expert * w.E and S <= fused
-        if decode_fused:
-            assert bench.launches_per_forward(w) == (1 if S <= one else 1 + 2), name
+        decode = w.fmt == "fp4" and w.act_fmt == "fp8" and S <= per_expert * w.E
+        if decode and S <= one:
+            assert bench.launches_per_forward(w) == 1, name
         else:
-            assert bench.launches_per_forward(w) == (2 if S <= single else 4) + 2 + 1, name
+            front = 2 if S <= single else 4
+            assert bench.launches_per_forward(w) == front + 2 + (0 if decode and S <= fused else 1), name
 
 
 def test_traffic_digest_ignores_comments_but_not_code(tmp_path, monkeypatch):

@@ -62,8 +62,8 @@ def test_deterministic_and_batch_invariant():
 def test_small_batch_matches_the_same_tokens_in_a_larger_batch():
     """240 slots and the same tokens inside a batch of 280: the same bits
     (the routing's padded layout moves, the rows' results do not). For FP4
-    decode batches, where the small batch also takes the fused routing +
-    quantization kernel, see test_fp4_fused_combine_matches_the_combine_kernel."""
+    decode batches, where the small batch also combines in GEMM2's epilogue,
+    see test_fp4_fused_combine_matches_the_combine_kernel."""
     wl = W.Workload("fused_vs_split", 120, 256, 256, 8, 2, "fp8", "zipf_sigmoid", seed=41, skip_frac=0.1)
     r = P.run_cuda(wl)
     extra = 20

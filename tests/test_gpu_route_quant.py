@@ -63,9 +63,8 @@ CASES = [
     P.W.scaled(P.W.WORKLOADS["dsv3_decode_fp8"], T=512, H=256, I=128),
     P.W.scaled(P.W.WORKLOADS["gptoss_fp8xfp4"], T=333, H=2880, I=128, E=16),
     P.W.scaled(P.W.WORKLOADS["dsv3_decode_fp4_T1"], H=512, I=256),
-    # FP8 weights, 256 and 264 slots: the separate routing (one CTA) and
-    # quantization kernels; FP4 decode batch of 256 slots: the fused
-    # small-batch routing + quantization kernel
+    # 256 and 264 slots: the single-CTA routing kernel; FP4 decode batch of
+    # 256 slots: the quantization kernel also sets up GEMM2's fused combine
     P.W.scaled(P.W.WORKLOADS["dsv3_decode_fp8"], T=32, H=256, I=128),
     P.W.scaled(P.W.WORKLOADS["dsv3_decode_fp8"], T=33, H=256, I=128),
     P.W.scaled(P.W.WORKLOADS["dsv3_decode_fp4_T32"], H=512, I=256),
@@ -134,8 +133,8 @@ def test_quantizer_exhaustive_bf16_sweep():
 @pytest.mark.parametrize("T,fmt,E", [(9, "fp8", 8), (70, "fp8", 8), (9, "fp4", 8), (40, "fp4", 64)])
 def test_duplicate_ids_in_one_token(T, fmt, E):
     """A token may name the same expert twice: each pair is routed on its own
-    (separate kernels for FP8 weights; for FP4 decode batches the single
-    launch at T=9 and the fused small-batch kernel at T=40)."""
+    (the routing kernel; for FP4 decode batches the single launch's own
+    routing at T=9, and the fused combine at T=40)."""
     wl = P.W.Workload("dups", T, 256, 128, E, 4, fmt, "softmax", seed=55)
     idx, w = P.W.make_routing(wl, "cuda")
     idx[0] = torch.tensor([3, 3, 3, 5], dtype=torch.int32)
