@@ -121,7 +121,7 @@ constexpr bool smem_layout_ok() {
          sizeof(S) + 1024 <= 227 * 1024 && kSfTmemCol + Pipe<DEC>::kStages * kSfColsPerStage<FMT> <= kTmemCols;
 }
 static_assert(smem_layout_ok<false, MOE_W_FP8>() && smem_layout_ok<false, MOE_W_FP4>() &&
-                  smem_layout_ok<true, MOE_W_FP4>() && smem_layout_ok<false, kMx>(),
+                  smem_layout_ok<true, MOE_W_FP4>() && smem_layout_ok<false, kMx>() && smem_layout_ok<true, kMx>(),
               "shared / tensor memory layout");
 
 struct TileCoord {
@@ -200,8 +200,8 @@ template <int FMT, int KIND, bool DEC>
 __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensorMap* tb1, const GemmArgs& a1,
                                           const CUtensorMap* ta2, const CUtensorMap* tb2, const GemmArgs& a2,
                                           const RqArgs* rq) {
-  static_assert(!DEC || FMT == MOE_W_FP4, "decode mode is built for FP4 weights");
-  static_assert(KIND != kBoth || DEC, "the single-launch forward runs the decode mode");
+  static_assert(!DEC || FMT != MOE_W_FP8, "decode mode is built for FP4 weights");
+  static_assert(KIND != kBoth || (DEC && FMT == MOE_W_FP4), "the single-launch forward runs the FP4 decode mode");
   using Smem = SmemT<DEC, FMT>;
   constexpr int kStages = Pipe<DEC>::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -282,13 +282,23 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
       if (tid == 0 && static_cast<int>(blockIdx.x) < __ldg(a1.tiles + 1) * g.NT) {
         const TileCoord c = tile_at(blockIdx.x);
         pre_unit = blockIdx.x;
-        pre_n = min(kStages, g.KB);
+        // FP4 activations: stages of two 128-K blocks (see the producer)
+        const int KS = (FMT == kMx) ? (g.KB + 1) / 2 : g.KB;
+        pre_n = min(kStages, KS);
         const int wrow = c.e * g.Np + c.nt * kBlockN;
         for (int s = 0; s < pre_n; ++s) {
-          mbar_arrive_expect_tx(&sm.full[s], kStageBytes);
-          tma_load_2d(sm.b[s], tb1, &sm.full[s], s * kBlockK, wrow);
-          bulk_load(sm.sfb[s], a1.w_scale + ((static_cast<size_t>(c.e) * g.NT + c.nt) * g.KB + s) * kSfbBytes,
-                    kSfbBytes, &sm.full[s]);
+          if constexpr (FMT == kMx) {
+            const int nch = min(2, g.KB - 2 * s);
+            mbar_arrive_expect_tx(&sm.full[s], Pipe<DEC>::kAStride + kTileBBytes + nch * (kSfaBytes + kSfbBytes));
+            tma_load_2d(sm.b[s], tb1, &sm.full[s], s * 128, wrow);
+            bulk_load(sm.sfb[s], a1.w_scale + ((static_cast<size_t>(c.e) * g.NT + c.nt) * g.KB + 2 * s) * kSfbBytes,
+                      nch * kSfbBytes, &sm.full[s]);
+          } else {
+            mbar_arrive_expect_tx(&sm.full[s], kStageBytes);
+            tma_load_2d(sm.b[s], tb1, &sm.full[s], s * kBlockK, wrow);
+            bulk_load(sm.sfb[s], a1.w_scale + ((static_cast<size_t>(c.e) * g.NT + c.nt) * g.KB + s) * kSfbBytes,
+                      kSfbBytes, &sm.full[s]);
+          }
         }
       }
     }
@@ -385,13 +395,18 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
           if (!mbar_wait(&sm.empty[stage], phase ^ 1, abort_flag)) break;
           if constexpr (FMT == kMx) {
             const int ch0 = 2 * kb, nch = min(2, KB - ch0);
-            mbar_arrive_expect_tx(&sm.full[stage], kTileABytes + kTileBBytes + nch * (kSfaBytes + kSfbBytes));
+            // decode mode: weight side already in flight from before the dependency wait
+            const bool pre = idx == pre_unit && kb < pre_n;
+            if (!pre)
+              mbar_arrive_expect_tx(&sm.full[stage],
+                                    Pipe<DEC>::kAStride + kTileBBytes + nch * (kSfaBytes + kSfbBytes));
             tma_load_2d(sm.a_stage(stage), TA, &sm.full[stage], kb * 128, c.row0);  // x in bytes
-            tma_load_2d(sm.b[stage], TB, &sm.full[stage], kb * 128, wrow);
+            if (!pre) tma_load_2d(sm.b[stage], TB, &sm.full[stage], kb * 128, wrow);
             bulk_load(sm.sfa[stage], A.a_sf + (static_cast<size_t>(c.row0 / kBlockM) * KB + ch0) * kSfaBytes,
                       nch * kSfaBytes, &sm.full[stage]);
-            bulk_load(sm.sfb[stage], A.w_scale + ((static_cast<size_t>(c.e) * NT + c.nt) * KB + ch0) * kSfbBytes,
-                      nch * kSfbBytes, &sm.full[stage]);
+            if (!pre)
+              bulk_load(sm.sfb[stage], A.w_scale + ((static_cast<size_t>(c.e) * NT + c.nt) * KB + ch0) * kSfbBytes,
+                        nch * kSfbBytes, &sm.full[stage]);
             if (++stage == kStages) { stage = 0; phase ^= 1; }
             continue;
           }
@@ -443,37 +458,61 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
             if (buf == 0) bphase ^= 1;
           }
         } else if constexpr (FMT == kMx) {
-          // tile mode, one issuing thread
-          if (!mbar_wait(&sm.tempty[0], bphase ^ 1, abort_flag)) break;
+          // one issuing thread (tile mode); in decode mode the warp walks the
+          // stages as for FP4 weights and moves the chunk's scale words
+          bool ok = mbar_wait(&sm.tempty[0], bphase ^ 1, abort_flag);
+          if constexpr (DEC) ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
           tc_fence_after();
-          bool ok = true;
+          int q = 0;
+          if constexpr (DEC) q = (tile_at(idx).row0 % kBlockM) / kChunkRows;
           const int KS = (KB + 1) / 2;
           for (int ks = 0; ks < KS; ++ks) {
-            if (!mbar_wait(&sm.full[stage], phase, abort_flag)) { ok = false; break; }
-            tc_fence_after();
+            bool okf = mbar_wait(&sm.full[stage], phase, abort_flag);
+            if constexpr (DEC) okf = __all_sync(0xffffffffu, okf);
+            if (!okf) { ok = false; break; }
             const int nch = min(2, KB - 2 * ks);
-            const uint32_t sfa_col = kSfTmemCol + stage * kSfColsPerStage<FMT>;
-            const uint32_t sfb_col = sfa_col + 8;
-            for (int ch = 0; ch < nch; ++ch) {
-              tmem_cp_32x128b_warpx4(tbase + sfa_col + 4 * ch,
-                                     smem_desc(smem_u32(sm.sfa[stage] + ch * kSfaBytes), 0, 128, kSwizzleNone));
-              tmem_cp_32x128b_warpx4(tbase + sfb_col + 8 * ch,
-                                     smem_desc(smem_u32(sm.sfb[stage] + ch * kSfbBytes), 0, 128, kSwizzleNone));
-              tmem_cp_32x128b_warpx4(tbase + sfb_col + 8 * ch + 4,
-                                     smem_desc(smem_u32(sm.sfb[stage] + ch * kSfbBytes + 512), 0, 128, kSwizzleNone));
+            if constexpr (DEC) {
+              if (q != 0) {
+                // the chunk's words are column q of each 128-row block image
+                for (int ch = 0; ch < nch; ++ch) {
+                  uint32_t* w = reinterpret_cast<uint32_t*>(sm.sfa[stage] + ch * kSfaBytes);
+                  const uint32_t v = w[4 * lane + q];
+                  __syncwarp();
+                  w[4 * lane] = v;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+              }
             }
-            const uint64_t ad = smem_desc(smem_u32(sm.a_stage(stage)), 16, 1024, kSwizzle128B);
-            const uint64_t bd = smem_desc(smem_u32(sm.b[stage]), 16, 1024, kSwizzle128B);
-            // four K = 64 steps of 32 bytes; step j takes scale bytes 2 (j % 2)
-            // and 2 (j % 2) + 1 of chunk j / 2
-            for (int j = 0; j < 2 * nch; ++j)
-              mma_mxf4(tbase, ad + 2 * j, bd + 2 * j, idesc_mxf4(kBlockM, kBlockN, 2 * (j & 1), 2 * (j & 1)),
-                       tbase + sfa_col + 4 * (j >> 1), tbase + sfb_col + 8 * (j >> 1), (ks > 0 || j > 0) ? 1u : 0u);
-            mma_commit(&sm.empty[stage]);
+            if (lane == 0) {
+              tc_fence_after();
+              const uint32_t sfa_col = kSfTmemCol + stage * kSfColsPerStage<FMT>;
+              const uint32_t sfb_col = sfa_col + 8;
+              for (int ch = 0; ch < nch; ++ch) {
+                tmem_cp_32x128b_warpx4(tbase + sfa_col + 4 * ch,
+                                       smem_desc(smem_u32(sm.sfa[stage] + ch * kSfaBytes), 0, 128, kSwizzleNone));
+                tmem_cp_32x128b_warpx4(tbase + sfb_col + 8 * ch,
+                                       smem_desc(smem_u32(sm.sfb[stage] + ch * kSfbBytes), 0, 128, kSwizzleNone));
+                tmem_cp_32x128b_warpx4(
+                    tbase + sfb_col + 8 * ch + 4,
+                    smem_desc(smem_u32(sm.sfb[stage] + ch * kSfbBytes + 512), 0, 128, kSwizzleNone));
+              }
+              const uint64_t ad = smem_desc(smem_u32(sm.a_stage(stage)), 16, 1024, kSwizzle128B);
+              const uint64_t bd = smem_desc(smem_u32(sm.b[stage]), 16, 1024, kSwizzle128B);
+              // four K = 64 steps of 32 bytes; step j takes scale bytes 2 (j % 2)
+              // and 2 (j % 2) + 1 of chunk j / 2
+              for (int j = 0; j < 2 * nch; ++j)
+                mma_mxf4(tbase, ad + 2 * j, bd + 2 * j, idesc_mxf4(kBlockM, kBlockN, 2 * (j & 1), 2 * (j & 1)),
+                         tbase + sfa_col + 4 * (j >> 1), tbase + sfb_col + 8 * (j >> 1),
+                         (ks > 0 || j > 0) ? 1u : 0u);
+              mma_commit(&sm.empty[stage]);
+            }
+            if constexpr (DEC) __syncwarp();
             if (++stage == kStages) { stage = 0; phase ^= 1; }
           }
           if (!ok) break;
-          mma_commit(&sm.tfull[0]);
+          if (lane == 0) mma_commit(&sm.tfull[0]);
           bphase ^= 1;
         } else {
           bool ok = mbar_wait(&sm.tempty[0], bphase ^ 1, abort_flag);
@@ -946,9 +985,13 @@ cudaError_t launch_gemm(int fmt, bool is_gemm1, bool decode, const CUtensorMap& 
   if (fmt == MOE_W_FP8)
     return is_gemm1 ? launch_one<MOE_W_FP8, true, false>(ta, tb, args, num_sms, st)
                     : launch_one<MOE_W_FP8, false, false>(ta, tb, args, num_sms, st);
-  if (fmt == kMx)
+  if (fmt == kMx) {
+    if (decode)
+      return is_gemm1 ? launch_one<kMx, true, true>(ta, tb, args, num_sms, st)
+                      : launch_one<kMx, false, true>(ta, tb, args, num_sms, st);
     return is_gemm1 ? launch_one<kMx, true, false>(ta, tb, args, num_sms, st)
                     : launch_one<kMx, false, false>(ta, tb, args, num_sms, st);
+  }
   if (decode)
     return is_gemm1 ? launch_one<MOE_W_FP4, true, true>(ta, tb, args, num_sms, st)
                     : launch_one<MOE_W_FP4, false, true>(ta, tb, args, num_sms, st);

@@ -42,12 +42,13 @@ PrepLayout prep_layout(int fmt, int E, const GemmGeom& g);
 GemmGeom geom_w13(int H, int I);
 GemmGeom geom_w2(int H, int I);
 
-// Decode mode (FP4 weights, at most kDecodePairsPerExpert pairs per expert
-// on average): 32-row token chunks in the GEMMs.
+// Decode mode (FP4 weights, with e4m3 or e2m1 activations, at most
+// kDecodePairsPerExpert pairs per expert on average): 32-row token chunks in
+// the GEMMs.
 constexpr int kDecodePairsPerExpert = 8;
 constexpr int kCombineSplits = 2;  // column halves of a GEMM2 tile row, finished by separate warpgroups
 inline bool decode_mode(int fmt, long long S, int E) {
-  return fmt == MOE_W_FP4 && S <= static_cast<long long>(kDecodePairsPerExpert) * E;
+  return (fmt == MOE_W_FP4 || fmt == MOE_W_FP4_ACT_FP4) && S <= static_cast<long long>(kDecodePairsPerExpert) * E;
 }
 
 struct WsLayout {
@@ -116,21 +117,26 @@ cudaError_t launch_quant(int fmt, const void* hidden, const float* topk_w, int T
 // kFusedCombineSlots slots. At larger decode batches the separate combine
 // kernel is faster (the epilogue's combines then hold up the accumulator
 // hand-back). The small-batch routing + quantization device code of the
-// single-launch forward is sized for the same batches.
+// single-launch forward is sized for the same batches. With FP4 activations
+// GEMM2 itself is faster and the threshold lower (DeepSeek-V3 shape, same
+// box: T=32, 256 slots, 0.397 ms with the fused combine against 0.390 in
+// tile mode with the combine kernel; T=8 0.185 against 0.189).
 constexpr int kFusedCombineSlots = 256;
+constexpr int kFusedCombineSlotsFp4Act = 64;
 inline bool fused_combine(int fmt, long long S, int E) {
-  return decode_mode(fmt, S, E) && S <= kFusedCombineSlots;
+  return decode_mode(fmt, S, E) && S <= (fmt == MOE_W_FP4_ACT_FP4 ? kFusedCombineSlotsFp4Act : kFusedCombineSlots);
 }
 // The whole forward as one cooperative launch (routing + quantization, then
 // the GEMM1 and GEMM2 units of one work list, GEMM2 units waiting on device
 // counters for their chunk's GEMM1 units; the combine in GEMM2's epilogue),
-// for fused-combine batches of at most kSingleLaunchSlots slots. Measured at
+// for FP4-weight (e4m3-activation) fused-combine batches of at most
+// kSingleLaunchSlots slots. Measured at
 // the DeepSeek-V3 shape (FP4, K = 8), one launch against the kernel
 // sequence: T=1 0.0652 vs 0.0706 ms, T=2 0.0942 vs 0.0971, T=4 0.1372 vs
 // 0.1380, T=8 0.2161 vs 0.2088, T=16 0.3549 vs 0.3263.
 constexpr int kSingleLaunchSlots = 32;
 inline bool single_launch(int fmt, long long S, int E) {
-  return fused_combine(fmt, S, E) && S <= kSingleLaunchSlots;
+  return fmt == MOE_W_FP4 && fused_combine(fmt, S, E) && S <= kSingleLaunchSlots;
 }
 cudaError_t launch_combine(const float* y, const int32_t* inv, int T, int H, int K, void* out, cudaStream_t st);
 // transposed: the weights are stored [E][K][N] (N contiguous) instead of [E][N][K].

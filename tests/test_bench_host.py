@@ -51,18 +51,22 @@ def test_launch_count_follows_the_library_thresholds():
     assert bench.launches_per_forward(wl(fused, 1, E, "fp8")) == 2 + 2 + 1
     assert bench.launches_per_forward(wl(fused, 1, E - 1, "fp4")) == 2 + 2 + 1  # not decode mode
     assert bench.launches_per_forward(wl(fused + 1, 1, 4 * E, "fp4")) == 2 + 2 + 1  # decode, separate combine
-    # FP4 activations: tile mode, separate combine
-    assert bench.launches_per_forward(W.scaled(wl(one, 1, E, "fp4"), act_fmt="fp4")) == 2 + 2 + 1
+    # FP4 activations: the decode mode, its fused combine up to `fused4` slots,
+    # no single launch
+    fused4 = _const("kFusedCombineSlotsFp4Act", "moe_internal.cuh")
+    assert bench.launches_per_forward(W.scaled(wl(fused4, 1, E, "fp4"), act_fmt="fp4")) == 2 + 2
+    assert bench.launches_per_forward(W.scaled(wl(fused4 + 1, 1, E, "fp4"), act_fmt="fp4")) == 2 + 2 + 1
     assert bench.launches_per_forward(W.scaled(wl(single + 1, 1, E, "fp4"), act_fmt="fp4")) == 4 + 2 + 1
     # every named workload is one of these cases
     for name, w in W.WORKLOADS.items():
         S = w.T * w.K
-        decode = w.fmt == "fp4" and w.act_fmt == "fp8" and S <= per_expert * w.E
-        if decode and S <= one:
+        decode = w.fmt == "fp4" and S <= per_expert * w.E
+        if decode and S <= one and w.act_fmt == "fp8":
             assert bench.launches_per_forward(w) == 1, name
         else:
             front = 2 if S <= single else 4
-            assert bench.launches_per_forward(w) == front + 2 + (0 if decode and S <= fused else 1), name
+            lim = fused4 if w.act_fmt == "fp4" else fused
+            assert bench.launches_per_forward(w) == front + 2 + (0 if decode and S <= lim else 1), name
 
 
 def test_traffic_digest_ignores_comments_but_not_code(tmp_path, monkeypatch):
