@@ -88,7 +88,9 @@ constexpr uint32_t kYBoxBytes = 32 * 16 * 4;
 template <bool DEC, int FMT>
 struct __align__(1024) SmemT {
   static constexpr int kSfChunks = FMT == kMx ? 2 : 1;  // 128-K scale chunks a stage
-  static constexpr int kSlots = FMT == kMx ? 1 : kScaleSlots;  // FP8 promotion-scale ring (FP8 only)
+  // slots of the FP8 promotion-scale ring below: unused by the FP4 formats,
+  // and shrunk for FP4 activations, whose larger scale stages need the room
+  static constexpr int kSlots = FMT == kMx ? 1 : kScaleSlots;
   uint8_t b[Pipe<DEC>::kStages][kTileBBytes];
   uint8_t a[Pipe<DEC>::kARegion];  // stage s at s * kAStride (1024-byte aligned)
   // GEMM2 in tile mode: per epilogue warp, a 32-row x 16-column fp32 box
