@@ -96,6 +96,27 @@ def test_fp4_requantization_bit_exact_on_the_epilogue_inputs(wl):
     assert (codes[:, wl.I:] == 0).all() and (exps[:, nb:] == 0).all()
 
 
+def test_fp4_activation_fused_combine_matches_the_combine_kernel():
+    """Decode batches of at most 64 slots combine in GEMM2's epilogue; the
+    same tokens inside a larger decode batch (120 slots) go through the
+    combine kernel: same bits, +0 rows for all-skipped tokens."""
+    wl = W.Workload("mx_fused_combine", 10, 320, 192, 64, 4, "fp4", "zipf_sigmoid", seed=48, skip_frac=0.2,
+                    act_fmt="fp4")
+    idx, w = W.make_routing(wl, "cuda")
+    idx[4] = -1
+    r = P.run_cuda(wl, idx=idx, w=w)
+    ref = P.oracle_out(r["hidden"], r["idx"], r["w"], r["weights"], None, act_fmt="fp4")
+    P.assert_close(r["out"], ref, "fused combine")
+    assert (r["out"][4].view(torch.int16) == 0).all()
+    extra = 20
+    g = torch.Generator(device="cuda").manual_seed(9)
+    hid = torch.cat([r["hidden"], torch.randn(extra, wl.H, generator=g, device="cuda").to(torch.bfloat16)])
+    idx2 = torch.cat([idx, torch.randint(0, wl.E, (extra, wl.K), generator=g, device="cuda", dtype=torch.int32)])
+    w2 = torch.cat([w, torch.rand(extra, wl.K, generator=g, device="cuda")])
+    out = P.B.experts_forward(hid, idx2, w2, r["prepared"])
+    assert torch.equal(out[:wl.T].view(torch.int16), r["out"].view(torch.int16))
+
+
 def test_fp4_activations_change_the_result():
     wl = CASES[3]
     r4 = P.run_cuda(wl)

@@ -26,17 +26,18 @@ def _static_call(wl, r, out):
     limit = float("nan") if wl.swiglu_limit is None else wl.swiglu_limit
     return B.lib().moe_experts_forward_static(
         r["hidden"].data_ptr(), r["idx"].data_ptr(), r["w"].data_ptr(), wl.T, wl.H, wl.I, wl.E, wl.K,
-        B.FMT[wl.fmt], p.w13_prep.data_ptr(), p.w2_prep.data_ptr(), ctypes.c_float(limit), out.data_ptr(),
+        B.FMT[p.fmt], p.w13_prep.data_ptr(), p.w2_prep.data_ptr(), ctypes.c_float(limit), out.data_ptr(),
         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
 @pytest.mark.parametrize("wl", [W.WORKLOADS["tiny_fp8"], W.WORKLOADS["dsv3_decode_fp4_T1"],
                                 W.Workload("fp4_small_clamp", 24, 256, 128, 8, 2, "fp4", "softmax", seed=41,
-                                           swiglu_limit=0.3)],
+                                           swiglu_limit=0.3),
+                                W.WORKLOADS["dsv3_decode_fp4xfp4_T1"]],
                          ids=lambda w: w.name)
 def test_static_workspace_forward_matches_workspace_forward(wl):
     r = P.run_cuda(wl)
-    assert B.lib().moe_workspace_bytes(B.FMT[wl.fmt], wl.T, wl.H, wl.I, wl.E, wl.K) <= \
+    assert B.lib().moe_workspace_bytes(B.FMT[P.lib_fmt(wl)], wl.T, wl.H, wl.I, wl.E, wl.K) <= \
         B.lib().moe_static_workspace_capacity()
     for call in range(2):
         out = torch.full_like(r["out"], float("nan"))
