@@ -237,7 +237,8 @@ def pack_e2m1(codes):
 def bf16_bits_to_f64(bits):
     """bf16 bit patterns (uint16) -> fp64 values (exact)."""
     b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
-    return b.view(np.float32).astype(np.float64)
+    with np.errstate(invalid="ignore"):  # NaN patterns stay NaN (no warning)
+        return b.view(np.float32).astype(np.float64)
 
 
 def f64_to_bf16_rne(v):
