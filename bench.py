@@ -166,10 +166,10 @@ def launches_per_forward(wl):
     routing (one kernel up to 8192 slots, else histogram + scan + scatter),
     the quantization kernel, GEMM1, GEMM2 and the combine (inside GEMM2 for
     FP4 weights with at most 8 pairs per expert and at most 256 slots, 64
-    with FP4 activations). FP4 activations never use the single launch."""
+    with FP4 activations)."""
     S = wl.T * wl.K
     decode = wl.fmt == "fp4" and S <= 8 * wl.E
-    if decode and S <= 32 and wl.act_fmt == "fp8":
+    if decode and S <= 32:
         return 1  # the single-launch decode forward
     combine = 0 if (decode and S <= (64 if wl.act_fmt == "fp4" else 256)) else 1
     return (2 if S <= 8192 else 4) + 2 + combine

@@ -377,7 +377,7 @@ moe_status bsmoe::forward_impl(const void* hidden, const int32_t* topk_idx, cons
     a1.chunk_ready = a2.chunk_ready = reinterpret_cast<int32_t*>(ws + L.chunk_ready);
     a2.ready_target = g1.NT;
     const RqArgs rq = make_rq_args(topk_idx, hidden, topk_w, T, H, E, K, L, ws, out);
-    if (launch_single_decode(ta1, tb1, ta2, tb2, a1, a2, rq, d.sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_single_decode(fmt, ta1, tb1, ta2, tb2, a1, a2, rq, d.sms, st) != cudaSuccess) return MOE_ERR_CUDA;
     for (int i = 1; i <= 5; ++i)
       if (!mark(i)) return MOE_ERR_CUDA;
     return MOE_OK;

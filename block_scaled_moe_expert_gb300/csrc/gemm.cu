@@ -203,7 +203,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
                                           const CUtensorMap* ta2, const CUtensorMap* tb2, const GemmArgs& a2,
                                           const RqArgs* rq) {
   static_assert(!DEC || FMT != MOE_W_FP8, "decode mode is built for FP4 weights");
-  static_assert(KIND != kBoth || (DEC && FMT == MOE_W_FP4), "the single-launch forward runs the FP4 decode mode");
+  static_assert(KIND != kBoth || DEC, "the single-launch forward runs the decode mode");
   using Smem = SmemT<DEC, FMT>;
   constexpr int kStages = Pipe<DEC>::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -267,7 +267,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
     RqSmem<kThreads / 32>& rs = *reinterpret_cast<RqSmem<kThreads / 32>*>(&sm.b[0][0]);
     route_small_in_smem<kThreads / 32>(rs, *rq);
     if (blockIdx.x == 0) write_routing<kThreads / 32>(rs, *rq);
-    quantize_tokens<kThreads / 32, true>(rs, *rq, blockIdx.x, gridDim.x);
+    quantize_tokens<kThreads / 32, true, FMT == kMx>(rs, *rq, blockIdx.x, gridDim.x);
     const int nchunks = rs.chs[rq->E];
     // the generic-proxy writes above (global: routing arrays, counters;
     // shared: the borrowed ring) are ordered before the TMA traffic below
@@ -352,24 +352,42 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
             asm volatile("fence.acq_rel.gpu;" ::: "memory");  // the relaxed read + fence acquire
             fence_proxy_async_global();
           } else {
-            const int npre = min(kStages, KB);
+            // (FP4 activations: a stage is two 128-K blocks, as below)
+            const int npre = min(kStages, (FMT == kMx) ? (KB + 1) / 2 : KB);
             const int st0 = stage;
             bool ok = true;
             for (int kb = 0; kb < npre; ++kb) {
               if (!mbar_wait(&sm.empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
-              mbar_arrive_expect_tx(&sm.full[stage], kStageBytes);
-              tma_load_2d(sm.b[stage], TB, &sm.full[stage], kb * kBlockK, wrow);
-              bulk_load(sm.sfb[stage], A.w_scale + ((static_cast<size_t>(c.e) * NT + c.nt) * KB + kb) * kSfbBytes,
-                        kSfbBytes, &sm.full[stage]);
+              if constexpr (FMT == kMx) {
+                const int nch = min(2, KB - 2 * kb);
+                mbar_arrive_expect_tx(&sm.full[stage],
+                                      Pipe<DEC>::kAStride + kTileBBytes + nch * (kSfaBytes + kSfbBytes));
+                tma_load_2d(sm.b[stage], TB, &sm.full[stage], kb * 128, wrow);
+                bulk_load(sm.sfb[stage],
+                          A.w_scale + ((static_cast<size_t>(c.e) * NT + c.nt) * KB + 2 * kb) * kSfbBytes,
+                          nch * kSfbBytes, &sm.full[stage]);
+              } else {
+                mbar_arrive_expect_tx(&sm.full[stage], kStageBytes);
+                tma_load_2d(sm.b[stage], TB, &sm.full[stage], kb * kBlockK, wrow);
+                bulk_load(sm.sfb[stage], A.w_scale + ((static_cast<size_t>(c.e) * NT + c.nt) * KB + kb) * kSfbBytes,
+                          kSfbBytes, &sm.full[stage]);
+              }
               if (++stage == kStages) { stage = 0; phase ^= 1; }
             }
             if (!ok || !wait_counter(ready, A.ready_target, abort_flag)) break;
             fence_proxy_async_global();
             for (int kb = 0; kb < npre; ++kb) {
               const int s = (st0 + kb) % kStages;
-              tma_load_2d(sm.a_stage(s), TA, &sm.full[s], kb * kBlockK, c.row0);
-              bulk_load(sm.sfa[s], A.a_sf + (static_cast<size_t>(c.row0 / kBlockM) * KB + kb) * kSfaBytes,
-                        kSfaBytes, &sm.full[s]);
+              if constexpr (FMT == kMx) {
+                const int nch = min(2, KB - 2 * kb);
+                tma_load_2d(sm.a_stage(s), TA, &sm.full[s], kb * 128, c.row0);
+                bulk_load(sm.sfa[s], A.a_sf + (static_cast<size_t>(c.row0 / kBlockM) * KB + 2 * kb) * kSfaBytes,
+                          nch * kSfaBytes, &sm.full[s]);
+              } else {
+                tma_load_2d(sm.a_stage(s), TA, &sm.full[s], kb * kBlockK, c.row0);
+                bulk_load(sm.sfa[s], A.a_sf + (static_cast<size_t>(c.row0 / kBlockM) * KB + kb) * kSfaBytes,
+                          kSfaBytes, &sm.full[s]);
+              }
             }
             kb0 = npre;
           }
@@ -382,7 +400,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
             // read the next unit's chunk counter ahead (its value is used at
             // that unit's start); placed a few stages in, so that the table
             // loads it needs do not delay this unit's first copies
-            if (kb == kb0 + 2 || (kb == kb0 && KB - kb0 <= 2)) {
+            if (kb == kb0 + 2 || (kb == kb0 && KS - kb0 <= 2)) {
               const int nidx = idx + static_cast<int>(gridDim.x);
               if (nidx >= U1 && nidx < total_tiles) {
                 const TileCoord nc = tile_at(nidx);
@@ -688,8 +706,14 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
       if (FMT == kMx && GEMM1) {
         // FP4 activations: SwiGLU, then the 1x32 e2m1 rule; a thread's 64
         // intermediate columns j = 128 nt + 64 wg + i are two whole blocks,
-        // so no exchange between the warpgroups is needed.
-        if (!ok) break;  // warp-uniform
+        // so no exchange between the warpgroups is needed. In the single
+        // launch every epilogue thread meets the release barrier below, so
+        // all of them stop together if any wait failed.
+        if constexpr (KIND == kBoth) {
+          if (epi_barrier_any(!ok)) break;
+        } else {
+          if (!ok) break;  // warp-uniform
+        }
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
           float gt = ACC(i), up = ACC(64 + i);
@@ -732,6 +756,13 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* ta1, const CUtensor
           // bytes 2 wg and 2 wg + 1 of the (row, 128-column block nt) scale word
           reinterpret_cast<uint16_t*>(args.out_sf)[2 * sf_word_index(row, c.nt, args.out_blocks) + wg] =
               static_cast<uint16_t>(ex);
+        }
+        if constexpr (KIND == kBoth) {
+          // release this unit's rows to the GEMM2 units of the chunk, as below
+          __threadfence();
+          fence_proxy_async_global();
+          epi_barrier_any(false);
+          if (tid == kEpiWarp0 * 32) atomicAdd(args.chunk_ready + c.row0 / kChunkRows, 1);
         }
       } else if (GEMM1) {
         // ACC(0..63) = gate, ACC(64..127) = up of intermediate columns
@@ -931,12 +962,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
 // The single-launch decode forward (FP4 weights, T * K <= 256): routing,
 // quantization, GEMM1 + SwiGLU + requantization, GEMM2 + routing weight +
 // the top-k combine, in one cooperative launch of one CTA per SM.
+template <int FMT>
 __global__ void __launch_bounds__(kThreads, 1)
 single_launch_decode_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constant__ CUtensorMap tb1,
                             const __grid_constant__ CUtensorMap ta2, const __grid_constant__ CUtensorMap tb2,
                             const __grid_constant__ GemmArgs a1, const __grid_constant__ GemmArgs a2,
                             const __grid_constant__ RqArgs rq) {
-  gemm_body<MOE_W_FP4, kBoth, true>(&ta1, &tb1, a1, &ta2, &tb2, a2, &rq);
+  gemm_body<FMT, kBoth, true>(&ta1, &tb1, a1, &ta2, &tb2, a2, &rq);
 }
 
 template <int FMT, bool GEMM1, bool DEC>
@@ -949,16 +981,16 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const GemmA
   return launch_kernel(true, kern, num_sms, kThreads, smem, st, ta, tb, args);
 }
 
-static_assert(sizeof(RqSmem<kThreads / 32>) <= sizeof(SmemT<true, MOE_W_FP4>::b),
+static_assert(sizeof(RqSmem<kThreads / 32>) <= sizeof(SmemT<true, MOE_W_FP4>::b) &&
+                  sizeof(RqSmem<kThreads / 32>) <= sizeof(SmemT<true, kMx>::b),
               "the routing + quantization phase borrows the weight ring");
 
-}  // namespace
-
-cudaError_t launch_single_decode(const CUtensorMap& ta1, const CUtensorMap& tb1, const CUtensorMap& ta2,
-                                 const CUtensorMap& tb2, const GemmArgs& a1, const GemmArgs& a2, const RqArgs& rq,
-                                 int num_sms, cudaStream_t st) {
-  auto kern = single_launch_decode_kernel;
-  const int smem = static_cast<int>(sizeof(SmemT<true, MOE_W_FP4>)) + 1024;
+template <int FMT>
+cudaError_t launch_single(const CUtensorMap& ta1, const CUtensorMap& tb1, const CUtensorMap& ta2,
+                          const CUtensorMap& tb2, const GemmArgs& a1, const GemmArgs& a2, const RqArgs& rq,
+                          int num_sms, cudaStream_t st) {
+  auto kern = single_launch_decode_kernel<FMT>;
+  const int smem = static_cast<int>(sizeof(SmemT<true, FMT>)) + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
@@ -980,6 +1012,15 @@ cudaError_t launch_single_decode(const CUtensorMap& ta1, const CUtensorMap& tb1,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, ta1, tb1, ta2, tb2, a1, a2, rq);
+}
+
+}  // namespace
+
+cudaError_t launch_single_decode(int fmt, const CUtensorMap& ta1, const CUtensorMap& tb1, const CUtensorMap& ta2,
+                                 const CUtensorMap& tb2, const GemmArgs& a1, const GemmArgs& a2, const RqArgs& rq,
+                                 int num_sms, cudaStream_t st) {
+  return fmt == kMx ? launch_single<kMx>(ta1, tb1, ta2, tb2, a1, a2, rq, num_sms, st)
+                    : launch_single<MOE_W_FP4>(ta1, tb1, ta2, tb2, a1, a2, rq, num_sms, st);
 }
 
 cudaError_t launch_gemm(int fmt, bool is_gemm1, bool decode, const CUtensorMap& ta, const CUtensorMap& tb,

@@ -129,14 +129,14 @@ inline bool fused_combine(int fmt, long long S, int E) {
 // The whole forward as one cooperative launch (routing + quantization, then
 // the GEMM1 and GEMM2 units of one work list, GEMM2 units waiting on device
 // counters for their chunk's GEMM1 units; the combine in GEMM2's epilogue),
-// for FP4-weight (e4m3-activation) fused-combine batches of at most
-// kSingleLaunchSlots slots. Measured at
+// for FP4-weight fused-combine batches of at most kSingleLaunchSlots slots
+// (either activation format). Measured at
 // the DeepSeek-V3 shape (FP4, K = 8), one launch against the kernel
 // sequence: T=1 0.0652 vs 0.0706 ms, T=2 0.0942 vs 0.0971, T=4 0.1372 vs
 // 0.1380, T=8 0.2161 vs 0.2088, T=16 0.3549 vs 0.3263.
 constexpr int kSingleLaunchSlots = 32;
 inline bool single_launch(int fmt, long long S, int E) {
-  return fmt == MOE_W_FP4 && fused_combine(fmt, S, E) && S <= kSingleLaunchSlots;
+  return fused_combine(fmt, S, E) && S <= kSingleLaunchSlots;
 }
 cudaError_t launch_combine(const float* y, const int32_t* inv, int T, int H, int K, void* out, cudaStream_t st);
 // transposed: the weights are stored [E][K][N] (N contiguous) instead of [E][N][K].
@@ -196,7 +196,7 @@ cudaError_t launch_gemm(int fmt, bool is_gemm1, bool decode, const CUtensorMap& 
 
 struct RqArgs;
 // The single-launch decode forward: one cooperative launch of num_sms CTAs.
-cudaError_t launch_single_decode(const CUtensorMap& ta1, const CUtensorMap& tb1, const CUtensorMap& ta2,
+cudaError_t launch_single_decode(int fmt, const CUtensorMap& ta1, const CUtensorMap& tb1, const CUtensorMap& ta2,
                                  const CUtensorMap& tb2, const GemmArgs& a1, const GemmArgs& a2, const RqArgs& rq,
                                  int num_sms, cudaStream_t st);
 

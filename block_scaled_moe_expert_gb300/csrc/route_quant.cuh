@@ -335,8 +335,9 @@ __device__ __forceinline__ void write_routing(RqSmem<kNW>& sm, const RqArgs& a) 
 }
 
 // Tokens t0, t0 + stride, ... : the valid slots' padded rows (ascending k),
-// the fused-combine setup, and the quantization into those rows.
-template <int kNW, bool kComplete>
+// the fused-combine setup, and the quantization into those rows (kFp4: the
+// e2m1 1x32 rule of the FP4-activation variant).
+template <int kNW, bool kComplete, bool kFp4>
 __device__ __forceinline__ void quantize_tokens(RqSmem<kNW>& sm, const RqArgs& a, int t0, int stride) {
   for (int t = t0; t < a.T; t += stride) {
     if (threadIdx.x == 0) {
@@ -355,8 +356,8 @@ __device__ __forceinline__ void quantize_tokens(RqSmem<kNW>& sm, const RqArgs& a
     const int n = sm.nrows;
     if (a.comb_cnt != nullptr) setup_combine(t, n, a.comb_cnt, a.comb_stride, a.out, a.H);
     if (n > 0)
-      quantize_token<kNW, kComplete>(a.hidden + static_cast<size_t>(t) * a.H, a.H, a.Kp, sm.rows, n, a.xq, a.xsf,
-                                     sm.qrow, sm.qsf);
+      quantize_token<kNW, kComplete, kFp4>(a.hidden + static_cast<size_t>(t) * a.H, a.H, a.Kp, sm.rows, n, a.xq, a.xsf,
+                                           sm.qrow, sm.qsf);
     __syncthreads();  // rows / nrows are rewritten for the next token
   }
 }

@@ -188,8 +188,8 @@ moe_status moe_prepare_weights_transposed(int fmt, int E, int H, int I, const vo
  * T*K <= 32 the whole forward is one cooperative launch of one CTA per SM
  * (GEMM2 work units wait on device counters for the GEMM1 units of their
  * rows), which needs every SM of the device free for the launch.
- * MOE_W_FP4_ACT_FP4 follows MOE_W_FP4 (decode mode; the combine in GEMM2,
- * for T*K <= 64 with this format) except that it never runs as one launch.
+ * MOE_W_FP4_ACT_FP4 follows MOE_W_FP4 (decode mode, the single launch; the
+ * combine in GEMM2 for T*K <= 64 with this format).
  */
 moe_status moe_experts_forward(const void* hidden, const int32_t* topk_idx, const float* topk_w, int T, int H,
                                int I, int E, int K, int fmt, const void* w13_prep, const void* w2_prep,
@@ -205,7 +205,7 @@ moe_status moe_experts_forward(const void* hidden, const int32_t* topk_idx, cons
  * memory). Where stages share a kernel the events between them are recorded
  * back to back: GEMM2 and the combine for FP4 weights with T*K <= 8E and
  * T*K <= 256 (T*K <= 64 for MOE_W_FP4_ACT_FP4) (events 4 and 5), and every stage
- * for MOE_W_FP4 with T*K <= 32 and T*K <= 8E, which run as one launch
+ * for FP4 weights with T*K <= 32 and T*K <= 8E, which run as one launch
  * (events 1 to 5 after it). Meant for
  * measuring the stages; errors as moe_experts_forward.
  */

@@ -51,9 +51,10 @@ def test_launch_count_follows_the_library_thresholds():
     assert bench.launches_per_forward(wl(fused, 1, E, "fp8")) == 2 + 2 + 1
     assert bench.launches_per_forward(wl(fused, 1, E - 1, "fp4")) == 2 + 2 + 1  # not decode mode
     assert bench.launches_per_forward(wl(fused + 1, 1, 4 * E, "fp4")) == 2 + 2 + 1  # decode, separate combine
-    # FP4 activations: the decode mode, its fused combine up to `fused4` slots,
-    # no single launch
+    # FP4 activations: the single launch up to `one` slots, the decode mode's
+    # fused combine up to `fused4` slots
     fused4 = _const("kFusedCombineSlotsFp4Act", "moe_internal.cuh")
+    assert bench.launches_per_forward(W.scaled(wl(one, 1, E, "fp4"), act_fmt="fp4")) == 1
     assert bench.launches_per_forward(W.scaled(wl(fused4, 1, E, "fp4"), act_fmt="fp4")) == 2 + 2
     assert bench.launches_per_forward(W.scaled(wl(fused4 + 1, 1, E, "fp4"), act_fmt="fp4")) == 2 + 2 + 1
     assert bench.launches_per_forward(W.scaled(wl(single + 1, 1, E, "fp4"), act_fmt="fp4")) == 4 + 2 + 1
@@ -61,7 +62,7 @@ def test_launch_count_follows_the_library_thresholds():
     for name, w in W.WORKLOADS.items():
         S = w.T * w.K
         decode = w.fmt == "fp4" and S <= per_expert * w.E
-        if decode and S <= one and w.act_fmt == "fp8":
+        if decode and S <= one:
             assert bench.launches_per_forward(w) == 1, name
         else:
             front = 2 if S <= single else 4
