@@ -670,10 +670,12 @@ def main():
         raise SystemExit(subprocess.call(plan[1]))
     from block_scaled_moe_expert_gb300 import workloads as W
     wl = W.WORKLOADS[args.workload]
+    # a changed shape is another workload: its name says so, and the per-launch
+    # DRAM record of the named workload does not apply to it
     if args.tokens:
-        wl = W.scaled(wl, T=args.tokens)
+        wl = W.scaled(wl, T=args.tokens, name=f"{wl.name}@T{args.tokens}")
     if args.experts:
-        wl = W.scaled(wl, E=args.experts)
+        wl = W.scaled(wl, E=args.experts, name=f"{wl.name}@E{args.experts}")
     if args.impl == "reference":
         run_reference(args, wl)
     else:

@@ -157,3 +157,21 @@ def test_gpus_flag_spawns_gloo_ranks():
     assert len(lines) == 1, r.stdout
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["config"]["parallelism"] == "replicas2"
+
+
+def test_shape_overrides_rename_the_workload(monkeypatch):
+    """--tokens / --experts give another workload: its name changes, so the
+    DRAM record of the named full-size workload is not reported for it."""
+    seen = {}
+
+    def fake_run(args, wl):
+        seen["wl"] = wl
+
+    monkeypatch.setattr(bench, "run_ours", fake_run)
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--workload", "dsv3_decode_fp4_T1", "--experts", "64",
+                                      "--tokens", "2"])
+    bench.main()
+    wl = seen["wl"]
+    assert (wl.T, wl.E) == (2, 64) and wl.name == "dsv3_decode_fp4_T1@T2@E64"
+    assert bench.measured_traffic(wl.name, "single_launch") is None
+    assert bench.measured_traffic("dsv3_decode_fp4_T1", "single_launch") is not None
