@@ -346,6 +346,81 @@ def _reference_line(args, wl, ws):
     print(json.dumps(line), flush=True)
 
 
+def rooflines(wl, stage_ms, pairs, touched, ms_step, peaks, peak_src, fp8):
+    """(roofline of the dominant kernel, roofline of the whole forward).
+
+    Dominant kernel: the single launch where one kernel runs the forward,
+    else the slower GEMM; its bound is the slower of its tensor-core time
+    (algorithmic flops / dense peak of the operand types) and its HBM time
+    (algorithmic bytes: touched-expert weights + activation rows in and out,
+    / the copy bandwidth). The whole forward takes max(flops / tensor peak,
+    bytes / HBM peak) with bytes = touched-expert weights (w13 + w2, codes
+    and scales) + hidden in + output out (bf16) + ids and routing weights.
+    """
+    flops = 6.0 * wl.H * wl.I * pairs
+    fbytes = (weight_bytes_per_expert(wl, 13) + weight_bytes_per_expert(wl, 2)) * touched \
+        + 2 * wl.T * wl.H * 2 + 8 * wl.T * wl.K
+    single = "single_launch" in stage_ms
+    if single:
+        # the single launch does the forward's work and moves its bytes
+        dom = "single_launch"
+        frac_1 = 1.0
+        kflops = flops
+        kbytes = fbytes
+    else:
+        dom = max(("gemm1", "gemm2"), key=lambda k: stage_ms[k])
+        frac_1 = 2.0 / 3.0 if dom == "gemm1" else 1.0 / 3.0
+        kflops = flops * frac_1
+        wb = weight_bytes_per_expert(wl, 13 if dom == "gemm1" else 2) * touched
+        # activation rows: e4m3 codes (e2m1, two per byte, with FP4
+        # activations) plus one 4-byte scale word per 128 columns
+        per = 2 if wl.act_fmt == "fp4" else 1
+        if dom == "gemm1":
+            act = pairs * (wl.H // per + 4 * ((wl.H + 127) // 128)) + pairs * (wl.I // per + 4 * ((wl.I + 127) // 128))
+        else:
+            act = pairs * (wl.I // per + 4 * ((wl.I + 127) // 128)) + pairs * wl.H * 4
+        kbytes = wb + act
+    peak_tc_2x = 2.0 * peaks["bf16_tflops"]  # fp8 dense = 2 x bf16 dense (nominal 4.5 / 2.25 PF)
+    if fp8 is not None:
+        peak_tc = fp8["tflops_burst"]
+        tc_src = (f"measured fp8: cuBLASLt e4m3 {fp8['n']}^3 GEMM, best of {fp8['reps']} "
+                  f"(profiles/fp8_peak.json); sustained {fp8['tflops_sustained']:.0f}")
+    else:
+        peak_tc = peak_tc_2x
+        tc_src = f"{peak_src}: 2 x bf16 burst (fp8/bf16 nominal ratio 2)"
+    if wl.act_fmt == "fp4":
+        # e2m1 x e2m1 runs at the FP4 tensor rate: the FP8 figure above times
+        # the nominal FP4 / FP8 dense ratio (13.5 / 4.5 PF)
+        peak_tc *= FP4_OVER_FP8
+        peak_tc_2x *= FP4_OVER_FP8
+        tc_src = f"fp4 = {FP4_OVER_FP8:g} x ({tc_src}), the nominal dense fp4/fp8 ratio"
+    peak_hbm = peaks["hbm_gbs"]
+    t_tc = kflops / (peak_tc * 1e12)
+    t_hbm = kbytes / (peak_hbm * 1e9)
+    secs = stage_ms[dom] * 1e-3
+    if t_tc >= t_hbm:
+        achieved = kflops / secs / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak_tc, "unit": "TFLOP/s",
+                "frac": achieved / peak_tc, "peak_source": tc_src,
+                "frac_vs_2x_bf16": achieved / peak_tc_2x, "frac_vs_spec_5pf": achieved / 5000.0}
+    else:
+        achieved = kbytes / secs / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak_hbm, "unit": "GB/s", "frac": achieved / peak_hbm,
+                "peak_source": f"{peak_src}: copy bandwidth", "frac_vs_spec_8tbs": achieved / 8000.0}
+    alg_units = (f"{frac_1:.3f} x 6*H*I*pairs flops = {kflops / 1e9:.1f} GFLOP; touched-expert weight + "
+                 f"{'hidden, output, ids and weights' if single else 'activation'} bytes = {kbytes / 1e9:.3f} GB; "
+                 f"roofline times tensor {t_tc * 1e3:.3f} ms, hbm {t_hbm * 1e3:.3f} ms")
+    traffic = measured_traffic(wl.name, dom)
+    roof.update({"kernel": dom, "traffic": traffic, "traffic_unit": "bytes per launch" if traffic else None,
+                 "kernel_ms": stage_ms[dom], "algorithmic": alg_units})
+    f_tc, f_hbm = flops / (peak_tc * 1e12), fbytes / (peak_hbm * 1e9)
+    fwd_roof = {"bound": "tensor" if f_tc >= f_hbm else "hbm", "roofline_ms": max(f_tc, f_hbm) * 1e3,
+                "tensor_ms": f_tc * 1e3, "hbm_ms": f_hbm * 1e3, "bytes": fbytes,
+                "frac": max(f_tc, f_hbm) * 1e3 / ms_step, "peaks": {"tensor_tflops": peak_tc, "hbm_gbs": peak_hbm}}
+    roof["forward_frac"] = fwd_roof["frac"]
+    return roof, fwd_roof
+
+
 def run_ours(args, wl):
     import torch
     from block_scaled_moe_expert_gb300 import binding as B
@@ -492,78 +567,12 @@ def run_ours(args, wl):
                "pipeline": "pinned host buffers; H2D and D2H on two copy streams overlapped with the "
                            "neighbouring steps' compute (2 buffer sets)"}
 
-    # Roofline of the dominant kernel: the slower of its tensor-core time
-    # (algorithmic flops / FP8 dense peak) and its HBM time (algorithmic
-    # bytes: touched-expert weights + activations in and out, / bandwidth).
-    single = launches_per_forward(wl) == 1
-    if single:
+    # Rooflines of the dominant kernel and of the whole forward
+    if launches_per_forward(wl) == 1:
         # one kernel runs the whole forward (its time lands in the first
-        # stage; the later events are recorded back to back): its work is
-        # the forward's flops and its bytes the forward's algorithmic bytes
-        dom = "single_launch"
-        stage_ms[dom] = stage_ms["route"]
-        frac_1 = 1.0
-        kflops = flops
-        kbytes = (weight_bytes_per_expert(wl, 13) + weight_bytes_per_expert(wl, 2)) * touched \
-            + 2 * wl.T * wl.H * 2 + 8 * wl.T * wl.K
-    else:
-        dom = max(("gemm1", "gemm2"), key=lambda k: stage_ms[k])
-        frac_1 = 2.0 / 3.0 if dom == "gemm1" else 1.0 / 3.0
-        kflops = flops * frac_1
-        wb = weight_bytes_per_expert(wl, 13 if dom == "gemm1" else 2) * touched
-        # activation rows: e4m3 codes (e2m1, two per byte, with FP4
-        # activations) plus one 4-byte scale word per 128 columns
-        per = 2 if wl.act_fmt == "fp4" else 1
-        if dom == "gemm1":
-            act = pairs * (wl.H // per + 4 * ((wl.H + 127) // 128)) + pairs * (wl.I // per + 4 * ((wl.I + 127) // 128))
-        else:
-            act = pairs * (wl.I // per + 4 * ((wl.I + 127) // 128)) + pairs * wl.H * 4
-        kbytes = wb + act
-    peak_tc_2x = 2.0 * peaks["bf16_tflops"]  # fp8 dense = 2 x bf16 dense (nominal 4.5 / 2.25 PF)
-    fp8 = load_fp8_peak()
-    if fp8 is not None:
-        peak_tc = fp8["tflops_burst"]
-        tc_src = (f"measured fp8: cuBLASLt e4m3 {fp8['n']}^3 GEMM, best of {fp8['reps']} "
-                  f"(profiles/fp8_peak.json); sustained {fp8['tflops_sustained']:.0f}")
-    else:
-        peak_tc = peak_tc_2x
-        tc_src = f"{peak_src}: 2 x bf16 burst (fp8/bf16 nominal ratio 2)"
-    if wl.act_fmt == "fp4":
-        # e2m1 x e2m1 runs at the FP4 tensor rate: the FP8 figure above times
-        # the nominal FP4 / FP8 dense ratio (13.5 / 4.5 PF)
-        peak_tc *= FP4_OVER_FP8
-        peak_tc_2x *= FP4_OVER_FP8
-        tc_src = f"fp4 = {FP4_OVER_FP8:g} x ({tc_src}), the nominal dense fp4/fp8 ratio"
-    peak_hbm = peaks["hbm_gbs"]
-    t_tc = kflops / (peak_tc * 1e12)
-    t_hbm = kbytes / (peak_hbm * 1e9)
-    secs = stage_ms[dom] * 1e-3
-    if t_tc >= t_hbm:
-        achieved = kflops / secs / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak_tc, "unit": "TFLOP/s",
-                "frac": achieved / peak_tc, "peak_source": tc_src,
-                "frac_vs_2x_bf16": achieved / peak_tc_2x, "frac_vs_spec_5pf": achieved / 5000.0}
-    else:
-        achieved = kbytes / secs / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peak_hbm, "unit": "GB/s", "frac": achieved / peak_hbm,
-                "peak_source": f"{peak_src}: copy bandwidth", "frac_vs_spec_8tbs": achieved / 8000.0}
-    alg_units = (f"{frac_1:.3f} x 6*H*I*pairs flops = {kflops / 1e9:.1f} GFLOP; touched-expert weight + "
-                 f"{'hidden, output, ids and weights' if single else 'activation'} bytes = {kbytes / 1e9:.3f} GB; "
-                 f"roofline times tensor {t_tc * 1e3:.3f} ms, hbm {t_hbm * 1e3:.3f} ms")
-    traffic = measured_traffic(wl.name, dom)
-    roof.update({"kernel": dom, "traffic": traffic, "traffic_unit": "bytes per launch" if traffic else None,
-                 "kernel_ms": stage_ms[dom], "algorithmic": alg_units})
-
-    # Whole-forward roofline: max(flops / tensor peak, bytes / HBM peak), with
-    # bytes = touched-expert weights (w13 + w2, codes and scales) + hidden in
-    # + output out (bf16) + ids and routing weights.
-    fbytes = (weight_bytes_per_expert(wl, 13) + weight_bytes_per_expert(wl, 2)) * touched \
-        + 2 * wl.T * wl.H * 2 + 8 * wl.T * wl.K
-    f_tc, f_hbm = flops / (peak_tc * 1e12), fbytes / (peak_hbm * 1e9)
-    fwd_roof = {"bound": "tensor" if f_tc >= f_hbm else "hbm", "roofline_ms": max(f_tc, f_hbm) * 1e3,
-                "tensor_ms": f_tc * 1e3, "hbm_ms": f_hbm * 1e3, "bytes": fbytes,
-                "frac": max(f_tc, f_hbm) * 1e3 / ms_step, "peaks": {"tensor_tflops": peak_tc, "hbm_gbs": peak_hbm}}
-    roof["forward_frac"] = fwd_roof["frac"]
+        # stage; the later events are recorded back to back)
+        stage_ms["single_launch"] = stage_ms["route"]
+    roof, fwd_roof = rooflines(wl, stage_ms, pairs, touched, ms_step, peaks, peak_src, load_fp8_peak())
 
     line = {"metric": METRIC, "value": replica_throughput(flops, world, ms_step * 1e-3) / 1e12, "unit": UNIT,
             "n_gpus": world,

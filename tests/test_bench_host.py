@@ -175,3 +175,49 @@ def test_shape_overrides_rename_the_workload(monkeypatch):
     assert (wl.T, wl.E) == (2, 64) and wl.name == "dsv3_decode_fp4_T1@T2@E64"
     assert bench.measured_traffic(wl.name, "single_launch") is None
     assert bench.measured_traffic("dsv3_decode_fp4_T1", "single_launch") is not None
+
+
+PEAKS = {"bf16_tflops": 2000.0, "hbm_gbs": 7000.0}
+FP8 = {"tflops_burst": 3500.0, "tflops_sustained": 3300.0, "n": 8192, "reps": 10}
+
+
+def test_roofline_tensor_bound_prefill_by_hand():
+    wl = W.WORKLOADS["mixtral_prefill_fp8"]  # H 4096, I 14336, 8 experts
+    sm = {"route": 0.02, "quant": 0.02, "gemm1": 0.75, "gemm2": 0.41, "combine": 0.03}
+    roof, fwd = bench.rooflines(wl, sm, 8192, 8, 1.25, PEAKS, "test", FP8)
+    flops1 = 4 * 4096 * 14336 * 8192  # GEMM1: 2 * pairs * H * 2I
+    assert roof["kernel"] == "gemm1" and roof["bound"] == "tensor" and roof["peak"] == 3500.0
+    assert abs(roof["achieved"] - flops1 / 0.75e-3 / 1e12) < 1e-9
+    assert abs(roof["frac_vs_2x_bf16"] - roof["achieved"] / 4000.0) < 1e-12
+    # forward: 6 H I pairs at 3500 TFLOP/s against 1.25 ms
+    assert fwd["bound"] == "tensor"
+    assert abs(fwd["frac"] - (6 * 4096 * 14336 * 8192 / 3500e12) / 1.25e-3) < 1e-12
+
+
+def test_roofline_hbm_bound_decode_by_hand():
+    wl = W.WORKLOADS["dsv3_decode_fp4_T128"]  # H 7168, I 2048, FP4 weights
+    sm = {"route": 0.015, "quant": 0.01, "gemm1": 0.52, "gemm2": 0.27, "combine": 0.012}
+    roof, _ = bench.rooflines(wl, sm, 1024, 190, 0.81, PEAKS, "test", FP8)
+    w13 = 4096 * 7168 // 2 + 4096 * (7168 // 32)  # e2m1 codes + one UE8M0 byte per 32
+    act = 1024 * (7168 + 4 * 56) + 1024 * (2048 + 4 * 16)  # e4m3 rows + scale words, in and out
+    assert roof["kernel"] == "gemm1" and roof["bound"] == "hbm" and roof["peak"] == 7000.0
+    assert abs(roof["achieved"] - (190 * w13 + act) / 0.52e-3 / 1e9) < 1e-6
+
+
+def test_roofline_fp4_activations_and_single_launch_by_hand():
+    wl = W.WORKLOADS["gptoss_fp4xfp4"]  # H = I = 2880, e2m1 activations
+    sm = {"route": 0.02, "quant": 0.04, "gemm1": 0.36, "gemm2": 0.21, "combine": 0.07}
+    roof, fwd = bench.rooflines(wl, sm, 32768, 128, 0.70, PEAKS, "test", FP8)
+    assert fwd["peaks"]["tensor_tflops"] == 3 * 3500.0  # FP4 rate: 3 x the FP8 figure
+    w13 = 5760 * 1440 + 5760 * 90
+    act = 32768 * (1440 + 4 * 23) + 32768 * (1440 + 4 * 23)  # e2m1 rows: half a byte per element
+    assert roof["bound"] == "hbm" and abs(roof["achieved"] - (128 * w13 + act) / 0.36e-3 / 1e9) < 1e-6
+    # one launch: the forward's flops and bytes against the launch's time
+    one = W.WORKLOADS["dsv3_decode_fp4_T1"]
+    sm1 = {"route": 0.066, "quant": 0.002, "gemm1": 0.002, "gemm2": 0.002, "combine": 0.002,
+           "single_launch": 0.066}
+    roof1, fwd1 = bench.rooflines(one, sm1, 8, 8, 0.066, PEAKS, "test", FP8)
+    per_expert = 3 * 7168 * 2048 // 2 + (4096 * 224 + 7168 * 64)
+    fbytes = 8 * per_expert + 2 * 7168 * 2 + 8 * 8
+    assert roof1["kernel"] == "single_launch" and fwd1["bytes"] == fbytes
+    assert abs(roof1["achieved"] - fbytes / 0.066e-3 / 1e9) < 1e-6
