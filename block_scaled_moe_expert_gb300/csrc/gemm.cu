@@ -959,9 +959,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
   gemm_body<FMT, GEMM1 ? kG1 : kG2, DEC>(&tmap_a, &tmap_b, args, &tmap_a, &tmap_b, args, nullptr);
 }
 
-// The single-launch decode forward (FP4 weights, T * K <= 256): routing,
-// quantization, GEMM1 + SwiGLU + requantization, GEMM2 + routing weight +
-// the top-k combine, in one cooperative launch of one CTA per SM.
+// The single-launch decode forward (FP4 weights, e4m3 or e2m1 activations;
+// sized for T * K <= 256, run for T * K <= 32): routing, quantization, GEMM1
+// + SwiGLU + requantization, GEMM2 + routing weight + the top-k combine, in
+// one cooperative launch of one CTA per SM.
 template <int FMT>
 __global__ void __launch_bounds__(kThreads, 1)
 single_launch_decode_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constant__ CUtensorMap tb1,
