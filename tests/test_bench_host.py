@@ -221,3 +221,17 @@ def test_roofline_fp4_activations_and_single_launch_by_hand():
     fbytes = 8 * per_expert + 2 * 7168 * 2 + 8 * 8
     assert roof1["kernel"] == "single_launch" and fwd1["bytes"] == fbytes
     assert abs(roof1["achieved"] - fbytes / 0.066e-3 / 1e9) < 1e-6
+
+
+def test_header_states_the_library_thresholds():
+    """The C header documents the batch sizes at which the forward changes
+    shape; they must be the library's constants."""
+    hdr = open(os.path.join(ROOT, "include", "moe_experts.h")).read()
+    hdr = re.sub(r"\s*\n\s*\*\s*", " ", hdr)  # join the comment lines
+    fused = _const("kFusedCombineSlots", "moe_internal.cuh")
+    fused4 = _const("kFusedCombineSlotsFp4Act", "moe_internal.cuh")
+    one = _const("kSingleLaunchSlots", "moe_internal.cuh")
+    per_expert = _const("kDecodePairsPerExpert", "moe_internal.cuh")
+    assert f"T*K <= {fused} and T*K <= {per_expert}E" in hdr or f"T*K <= {per_expert}E and T*K <= {fused}" in hdr
+    assert f"T*K <= {fused4} for MOE_W_FP4_ACT_FP4" in hdr
+    assert f"T*K <= {one} and T*K <= {per_expert}E" in hdr
